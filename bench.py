@@ -1,0 +1,391 @@
+#!/usr/bin/env python3
+"""Benchmark of the Split-KV anchor-attention hot path on GB300.
+
+One step = one pass of the whole path over one synthetic batch, all through
+the C ABI: chunk prices (Eq. 6) -> LPT plan -> per-rank partial attention
+(Eq. 3) -> LSE merge (Eq. 4) -> backward (Alg. 1), with the inputs resident in
+HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU fp64 oracle, timed on the host cores
+
+With N > 1 (torchrun) every rank runs an independent replica of the workload
+(weak scaling, no collective on the data path); value = work of all ranks /
+the slowest rank's time.
+"""
+import os
+
+# BLAS threads of the oracle legs: every host core (set before numpy loads).
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+
+import argparse
+import json
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "anchor-attn fwd+bwd useful TFLOP/s and % BF16 tensor peak; merge HBM GB/s"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "packed_4x128k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def useful_pairs_per_head(s, a, B):
+    return int(B * (a.long() - s.long()).clamp(min=0).sum().item())
+
+
+# ------------------------------------------------------------------ oracle legs
+
+def oracle_sample(w, inp, budget_s: float, block_offset: int = 0):
+    """Times the CPU oracle (as it stands) on a bounded sample of the workload:
+    forward (+ backward when the workload has one) of whole query blocks of one
+    head, until ~budget_s seconds of work.  Returns (TFLOP/s useful, desc)."""
+    import oracle as orc
+    N = w.N
+    stride = max(1, N // 64)
+    order = [(block_offset + t * stride) % N for t in range(N)]
+    head = 0
+    t0 = time.perf_counter()
+    pairs = 0
+    done = []
+    for i in order:
+        orc.attention_forward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, blocks=[i], heads=[head])
+        if w.backward:
+            orc.attention_backward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, inp.dO, blocks=[i], heads=[head])
+        pairs += w.B * max(0, int(inp.a[i]) - int(inp.s[i]))
+        done.append(i)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    flops = pairs * w.d * (12 if w.backward else 4)
+    desc = (f"{len(done)} query blocks (B={w.B} rows each) x head {head} of {w.name}, "
+            f"{'fwd+bwd' if w.backward else 'fwd'}, {pairs} useful pairs, {dt:.1f} s")
+    return flops / dt / 1e12, desc, dt
+
+
+def blas_threads():
+    v = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    try:
+        return int(v)
+    except (TypeError, ValueError):
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    per_step = []
+    for t in range(args.warmup + args.steps):
+        tf, desc, dt = oracle_sample(w, inp, args.ref_step_s, block_offset=7 * t)
+        if t >= args.warmup:
+            per_step.append((tf, dt, desc))
+    value = statistics.mean(x[0] for x in per_step)
+    ms = statistics.mean(x[1] for x in per_step) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "S": w.S, "Q": w.Q, "H": w.H, "d": w.d, "P": w.P, "order": w.order,
+                   "sample": "bounded oracle sample per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                         "sample": per_step[-1][2]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    from lse_merge_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        dist.barrier()
+    import lse_merge_gb300 as skv
+    from lse_merge_gb300 import _lib
+    from workloads import WORKLOADS, make_inputs
+
+    lib = _lib.load()
+    w = WORKLOADS[args.workload]
+    if world > 1:
+        w = w.with_(seed=w.seed + 1000 * rank)     # independent replica per rank
+    inp = make_inputs(w, with_grad=w.backward, pin=True)
+    dev = torch.device("cuda", local_rank)
+    tdt = torch.float32 if w.dtype == "fp32" else torch.bfloat16
+    s, a = inp.s.to(dev), inp.a.to(dev)
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    dO = inp.dO.to(dev) if w.backward else None
+    prob = skv.Problem(s, a, w.B, w.H, w.d, w.S, w.m, w.P, tdt)
+    P, Q, H, d = w.P, w.Q, w.H, w.d
+    o_part = torch.empty(P, Q, H, d, dtype=torch.float32, device=dev)
+    lse_part = torch.empty(P, Q, H, dtype=torch.float32, device=dev)
+    o = torch.empty(Q, H, d, dtype=tdt, device=dev)
+    lse = torch.empty(Q, H, dtype=torch.float32, device=dev)
+    if w.backward:
+        dq = torch.empty(Q, H, d, dtype=torch.float32, device=dev)
+        dk = torch.empty(w.S, H, d, dtype=torch.float32, device=dev)
+        dv = torch.empty(w.S, H, d, dtype=torch.float32, device=dev)
+        ws_b = torch.empty(skv.workspace_bytes(prob, 1), dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(skv.workspace_bytes(prob, 0), dtype=torch.uint8, device=dev)
+    costs = torch.empty(w.n_chunks, dtype=torch.int64, device=dev)
+
+    def path(ev=None):
+        if ev: ev[0].record()
+        skv.chunk_costs(prob, costs)
+        if w.order == "lpt":
+            roc, _, _ = skv.lpt_order(costs, P, w.J)
+        else:
+            roc, _, _ = skv.contiguous_order(w.n_chunks, P, w.J, costs)
+        if ev: ev[1].record()
+        skv.attn_fwd(prob, q, k, v, roc, o_part, lse_part, ws_f)
+        if ev: ev[2].record()
+        skv.lse_merge(o_part, lse_part, o=o, lse=lse)
+        if ev: ev[3].record()
+        if w.backward:
+            skv.attn_bwd(prob, q, k, v, o, lse, dO, roc, dq, dk, dv, ws_b)
+        if ev: ev[4].record()
+
+    for _ in range(args.warmup):
+        path()
+    torch.cuda.synchronize()
+    st = skv.stream_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n0 = lib.skv_launch_count()
+    clocks.start()
+    time.sleep(0.3)
+    start.record()
+    for t in range(args.steps):
+        path(evs[t])
+    end.record()
+    torch.cuda.synchronize()
+    launches = lib.skv_launch_count() - n0
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = start.elapsed_time(end) / args.steps
+    ph = {"plan": [], "fwd": [], "merge": [], "bwd": []}
+    for e in evs:
+        ph["plan"].append(e[0].elapsed_time(e[1]))
+        ph["fwd"].append(e[1].elapsed_time(e[2]))
+        ph["merge"].append(e[2].elapsed_time(e[3]))
+        ph["bwd"].append(e[3].elapsed_time(e[4]))
+    ph = {kk: statistics.mean(vv) for kk, vv in ph.items()}
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    if skv.stream_status() != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    pairs = useful_pairs_per_head(inp.s, inp.a, w.B) * H
+    fwd_flops = 4.0 * d * pairs
+    bwd_flops = 8.0 * d * pairs if w.backward else 0.0
+    step_flops = fwd_flops + bwd_flops
+    value = step_flops * world / (ms * 1e-3) / 1e12
+    pk, pk_kind = peaks()
+    sustained = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    finite = int(torch.isfinite(lse_part).sum().item())
+    out_b = 2 if tdt == torch.bfloat16 else 4
+    merge_bytes = P * Q * H * 4 + finite * d * 4 + Q * H * (d * out_b + 4)
+    merge_gbs = merge_bytes / (ph["merge"] * 1e-3) / 1e9
+    attn = {"fwd": (fwd_flops, ph["fwd"])}
+    if w.backward:
+        attn["bwd"] = (bwd_flops, ph["bwd"])
+    dom = max(attn, key=lambda x: attn[x][1])
+    dom_tf = attn[dom][0] / (attn[dom][1] * 1e-3) / 1e12
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        with open(tr_path) as f:
+            tr = json.load(f).get(w.name, {}).get(dom)
+        traffic = tr if tr else None
+
+    # end to end through the public API with host buffers (pinned), copies inside
+    e2e = None
+    if not args.no_e2e and w.backward:
+        h_o = torch.empty(Q, H, d, dtype=tdt, pin_memory=True)
+        h_lse = torch.empty(Q, H, dtype=torch.float32, pin_memory=True)
+        h_dq = torch.empty(Q, H, d, dtype=torch.float32, pin_memory=True)
+        h_dk = torch.empty(w.S, H, d, dtype=torch.float32, pin_memory=True)
+        h_dv = torch.empty(w.S, H, d, dtype=torch.float32, pin_memory=True)
+        h_in = [(inp.s, s), (inp.a, a), (inp.q, q), (inp.k, k), (inp.v, v), (inp.dO, dO)]
+        h_out = [(o, h_o), (lse, h_lse), (dq, h_dq), (dk, h_dk), (dv, h_dv)]
+        bi = sum(x.numel() * x.element_size() for x, _ in h_in)
+        bo = sum(x.numel() * x.element_size() for x, _ in h_out)
+
+        def e2e_step():
+            for hsrc, ddst in h_in:
+                ddst.copy_(hsrc, non_blocking=True)
+            path()
+            for dsrc, hdst in h_out:
+                hdst.copy_(dsrc, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        ke = max(1, min(args.steps, 3))
+        t_s, t_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_s.record()
+        for _ in range(ke):
+            e2e_step()
+        t_e.record()
+        torch.cuda.synchronize()
+        e_ms = t_s.elapsed_time(t_e) / ke
+        if world > 1:
+            tt = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": step_flops * world / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, desc, _ = oracle_sample(w, inp, args.cpu_budget_s)
+        cpu = {"value": tf, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if tdt == torch.bfloat16 else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "b": w.n_samples, "S": w.S, "Q": w.Q, "B": w.B, "H": H, "d": d,
+                       "m": w.m, "P": P, "J": w.J, "order": w.order,
+                       "l2": "inputs larger than L2 (K+V alone exceed 129 MB)",
+                       "parallelism": f"{world} independent replica(s)"},
+            "pct_bf16_peak": {"measured_sustained": value / world / sustained,
+                              "nominal_2250": value / world / 2250.0},
+            "phases_ms": ph,
+            "useful_tflop_per_step": step_flops / 1e12,
+            "merge": {"gbs": merge_gbs, "bytes": merge_bytes, "frac_of_hbm": merge_gbs / hbm,
+                      "peak_gbs": hbm, "peak_kind": pk_kind},
+            "roofline": {"kernel": f"attn_{dom}", "bound": "tensor", "achieved": dom_tf,
+                         "peak": sustained, "unit": "TFLOP/s", "frac": dom_tf / sustained,
+                         "peak_kind": f"{pk_kind} sustained bf16", "traffic": traffic},
+            "gpu_launches": int(launches),
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--ref-step-s", type=float, default=4.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,226 @@
+/*
+ * skv.h -- C ABI of libskv, the GB300 (sm_103a) Split-KV anchor-attention path.
+ *
+ * Method: "Split-KV: Efficient Context Parallelism for Training Diffusion
+ * Drafters" (Zhang, Zhang, Xie, Fan, You), cited as [Split-KV ...].
+ *
+ * The path, per training step: price the context chunks (Eq. 6), balance them
+ * over P virtual ranks with cost-aware LPT (§4.2), compute every rank's local
+ * partial attention (o_p, l_p) (Eq. 3, Alg. 1 line 7), merge the partials
+ * exactly (Eq. 4, Alg. 1 line 8) and run the backward (Alg. 1 lines 12-21),
+ * all on one GPU: the P ranks are a sweep over key/value chunks, and the
+ * collectives of Alg. 1 become on-device passes.
+ *
+ * Conventions shared by every call
+ *  - Pointers named "device" point to GPU global memory owned by the caller;
+ *    the library never allocates, frees or keeps a pointer after a call
+ *    returns.  Host pointers (the skv_problem struct itself) are read during
+ *    the call only.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    asynchronous on that stream; outputs are valid once the stream reaches
+ *    the call.
+ *  - Scalar arguments are validated on the host before any launch: a bad one
+ *    returns SKV_ERR_INVALID_ARG or SKV_ERR_UNSUPPORTED and launches nothing.
+ *  - Anchor metadata is checked on the device (skv_chunk_costs): violations
+ *    raise SKV_ERR_BAD_ANCHORS in the per-process device status word, read by
+ *    skv_stream_status.  Kernels clamp every index they derive from anchors,
+ *    so bad metadata yields wrong numbers, never an out-of-bounds access.
+ *  - Layouts are row-major.  Query tensors are [Q][H][d] (Q = n_blocks * B),
+ *    context tensors [S][H][d]; query row r belongs to block floor(r / B).
+ */
+#ifndef SKV_H_
+#define SKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SKV_API __attribute__((visibility("default")))
+#else
+#define SKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum skv_status {
+    SKV_OK = 0,
+    SKV_ERR_INVALID_ARG = 1,   /* a scalar or pointer argument is invalid */
+    SKV_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim) */
+    SKV_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    SKV_ERR_TIMEOUT = 4,       /* a bounded on-device wait ran out (device status) */
+    SKV_ERR_BAD_ANCHORS = 5,   /* anchor metadata violates 0 <= s_i <= a_i <= S (device status) */
+    SKV_ERR_WORKSPACE = 6      /* workspace pointer NULL/misaligned or smaller than skv_workspace_bytes */
+} skv_status;
+
+typedef enum skv_dtype {
+    SKV_FP32 = 0,              /* float */
+    SKV_BF16 = 1               /* bfloat16 (IEEE-754 binary32 upper half) */
+} skv_dtype;
+
+/*
+ * One anchor-attention problem [Split-KV §3.1, Fig. 1; §4.2].
+ * Block i (rows [i*B, (i+1)*B)) attends exactly the context keys
+ * s_i <= x < a_i.  The context [0, S) is cut into S/m chunks
+ * [j*m, (j+1)*m); P virtual ranks hold J chunks each (P*J*m == S).
+ */
+typedef struct skv_problem {
+    int32_t B;            /* block size: query rows per anchor, 1..128        */
+    int32_t n_blocks;     /* N (>= 0); Q = N*B query rows                      */
+    int32_t n_heads;      /* H >= 1                                            */
+    int32_t head_dim;     /* d in {64, 128}                                    */
+    int64_t S;            /* packed context length >= 1                        */
+    int32_t m;            /* chunk length >= 1 (attention: a multiple of 128)  */
+    int32_t P;            /* virtual ranks >= 1                                */
+    int32_t J;            /* chunks per rank; P*J*m must equal S               */
+    const int32_t* s;     /* device [N]: sample start of block i               */
+    const int32_t* a;     /* device [N]: anchor of block i, s_i <= a_i <= S    */
+    skv_dtype dtype;      /* dtype of q, k, v, o (merged) and dO               */
+    float scale;          /* softmax scale; 0 selects 1/sqrt(head_dim)         */
+} skv_problem;
+
+/*
+ * Chunk prices, [Split-KV §4.2, Eq. 6]:
+ *   costs[j] = B * sum_i (min(a_i, j*m + m) - max(s_i, j*m))^+ ,  j < S/m.
+ * costs: device int64[S/m], written.  Exact integer arithmetic.  Also checks
+ * 0 <= s_i <= a_i <= S for every block (SKV_ERR_BAD_ANCHORS in the device
+ * status word; offending blocks are clamped into range before pricing).
+ */
+SKV_API skv_status skv_chunk_costs(const skv_problem* prob, int64_t* costs, void* stream);
+
+/*
+ * Cost-aware LPT [Split-KV §4.2 "Cost-aware LPT"]: chunks are taken in order of
+ * (cost descending, chunk index ascending); each goes to the rank with the
+ * smallest (load, rank index) among ranks holding fewer than J chunks.  The
+ * final locality matching is the identity (bundle p is rank p).
+ *   costs         device int64[n_chunks], read (n_chunks == P*J <= 16384,
+ *                 P <= 1024; larger plans return SKV_ERR_UNSUPPORTED)
+ *   rank_of_chunk device int32[n_chunks], written: rank of chunk j
+ *   order         device int32[n_chunks], written: rank-major chunk lists,
+ *                 order[p*J .. p*J+J) are rank p's chunks in assignment order
+ *   load          device int64[P], written: C_p = sum of its chunks' costs
+ * Exact integer arithmetic; one thread block.
+ */
+SKV_API skv_status skv_lpt_order(const int64_t* costs, int32_t n_chunks, int32_t P, int32_t J,
+                         int32_t* rank_of_chunk, int32_t* order, int64_t* load, void* stream);
+
+/*
+ * "No balance" baseline [Split-KV §5.1 Baselines]: chunk j goes to rank j / J.
+ * Same outputs as skv_lpt_order; costs may be NULL, in which case load may be
+ * NULL too (otherwise load[p] = sum of rank p's costs).
+ */
+SKV_API skv_status skv_contiguous_order(const int64_t* costs, int32_t n_chunks, int32_t P, int32_t J,
+                                int32_t* rank_of_chunk, int32_t* order, int64_t* load,
+                                void* stream);
+
+/*
+ * Zigzag baseline [Split-KV §4.2 "A concrete example", Fig. 5b]: every sample of
+ * length L is cut into 2P chunks of L/(2P) positions; rank p receives chunks p
+ * and 2P-1-p of each sample.  Returns per-rank context loads C_p only (Zigzag
+ * chunks are not the m-sized chunks the attention kernels consume).
+ *   sample_start, sample_len  device int32[n_samples]; every sample_len must be
+ *                             a multiple of 2P and the samples must lie in [0, S)
+ *   load                      device int64[P], written
+ */
+SKV_API skv_status skv_zigzag_loads(const skv_problem* prob, const int32_t* sample_start,
+                            const int32_t* sample_len, int32_t n_samples,
+                            int64_t* load, void* stream);
+
+/*
+ * Workspace size in bytes of skv_attn_fwd (which = 0) or skv_attn_bwd
+ * (which = 1) for this problem; 0 if the problem is invalid.  The caller
+ * allocates it (256-byte aligned) and may reuse it across calls on one stream.
+ */
+SKV_API size_t skv_workspace_bytes(const skv_problem* prob, int which);
+
+/*
+ * Local partial attention of every virtual rank [Split-KV §4.1, Eq. 3;
+ * Alg. 1 line 7]: for each rank p, each query row r and head h,
+ *   z_x = scale * q_r . k_x  over the keys x in K_p with s_i <= x < a_i,
+ *   lse_part[p][r][h] = log sum_x exp(z_x)          (natural log)
+ *   o_part[p][r][h][:] = sum_x exp(z_x - lse) v_x
+ * K_p is the union of the chunks whose rank_of_chunk equals p (any map into
+ * [0, P) is accepted; entries outside it are ignored and flag
+ * SKV_ERR_INVALID_ARG in the device status word).  Rows with no visible key in
+ * K_p get lse_part = -inf; their o_part row is unspecified (never read by
+ * skv_lse_merge).
+ *   q             device [Q][H][d], dtype prob->dtype
+ *   k, v          device [S][H][d], dtype prob->dtype; rows 16-byte aligned
+ *   rank_of_chunk device int32[S/m]
+ *   o_part        device float[P][Q][H][d], written
+ *   lse_part      device float[P][Q][H], written
+ *   workspace     device, >= skv_workspace_bytes(prob, 0) bytes
+ * bf16 problems run on the tcgen05 tensor cores (bf16 products, fp32
+ * accumulation); fp32 problems run an fp32 CUDA-core kernel.
+ */
+SKV_API skv_status skv_attn_fwd(const skv_problem* prob, const void* q, const void* k, const void* v,
+                        const int32_t* rank_of_chunk, float* o_part, float* lse_part,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Exact LSE merge of P disjoint partials [Split-KV §4.1, Eq. 4; Alg. 1 line 8]:
+ *   lse[r] = log sum_p exp(lse_part[p][r]),
+ *   o[r][:] = sum_p exp(lse_part[p][r] - lse[r]) * o_part[p][r][:].
+ * Partials with lse_part = -inf are skipped (their o_part row is not read);
+ * a row whose partials are all -inf gets o = 0, lse = -inf.
+ *   o_part   device float[P][rows][head_dim]  (rows = Q*H for attention)
+ *   lse_part device float[P][rows]
+ *   o        device [rows][head_dim] of o_dtype, written (bf16: round to nearest even)
+ *   lse      device float[rows], written (may be NULL)
+ * head_dim must be a multiple of 4 (<= 256); o_part 16-byte aligned.
+ */
+SKV_API skv_status skv_lse_merge(const float* o_part, const float* lse_part, int32_t P, int64_t rows,
+                         int32_t head_dim, void* o, skv_dtype o_dtype, float* lse, void* stream);
+
+/*
+ * Backward of the merged attention for L = sum(dO * o), lse receiving no
+ * gradient [Split-KV Alg. 1 lines 12-21]: each virtual rank p produces dq^(p)
+ * and the dk_p, dv_p rows of its own chunks (the keys it holds); dq is the sum
+ * of the dq^(p) over ranks (Alg. 1 line 17, made local).  The per-rank
+ * MERGE_BWD of Alg. 1 line 15 is taken in its merged form: with
+ * D_r = dO_r . o_r and the global lse, the score gradient on rank p is
+ * P_rx (dO_r . v_x - D_r) with P_rx = exp(z_rx - lse_r), which equals the
+ * per-rank route exactly.
+ *   q, dO     device [Q][H][d], dtype prob->dtype
+ *   k, v      device [S][H][d], dtype prob->dtype
+ *   o         device [Q][H][d], dtype prob->dtype (the merged output)
+ *   lse       device float[Q][H] (the merged log-sum-exp, natural log)
+ *   dq        device float[Q][H][d], written
+ *   dk, dv    device float[S][H][d], written (keys no query sees get 0)
+ *   workspace device, >= skv_workspace_bytes(prob, 1) bytes
+ */
+SKV_API skv_status skv_attn_bwd(const skv_problem* prob, const void* q, const void* k, const void* v,
+                        const void* o, const float* lse, const void* dO,
+                        const int32_t* rank_of_chunk, float* dq, float* dk, float* dv,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device (SKV_ERR_BAD_ANCHORS, SKV_ERR_TIMEOUT, SKV_ERR_INVALID_ARG
+ * raised by kernels), or SKV_ERR_CUDA if the stream reports a CUDA error.
+ * The word is shared by all streams of the process on that device.
+ */
+SKV_API skv_status skv_stream_status(void* stream);
+
+/* Static English name of a status code. */
+SKV_API const char* skv_status_str(skv_status status);
+
+/*
+ * Test hook: iteration cap of every bounded on-device wait of the tensor-core
+ * kernels on the current device (default 2^31).  A wait that runs out sets
+ * SKV_ERR_TIMEOUT, abandons the work item and lets the kernel finish cleanly.
+ * `limit` <= 0 restores the default.
+ */
+SKV_API skv_status skv_set_wait_limit(int64_t limit);
+
+/*
+ * Number of kernels this library has launched in the process so far (all
+ * devices, all streams; host-side counter, incremented per launch).
+ */
+SKV_API uint64_t skv_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SKV_H_ */

@@ -1,0 +1,38 @@
+// Internal launcher declarations shared by the libskv translation units.
+#pragma once
+
+#include "skv_common.cuh"
+
+namespace skv_internal {
+
+constexpr int kLptMaxChunks = 16384;   // LPT sorts in shared memory
+constexpr int kLptMaxRanks = 1024;     // LPT greedy keeps ranks in one warp's registers
+
+skv_status launch_chunk_costs(const skv_problem& pb, int64_t* costs, const skv_host::Ctx& c);
+skv_status launch_lpt(const int64_t* costs, int n, int P, int J, int32_t* roc, int32_t* order,
+                      int64_t* load, const skv_host::Ctx& c);
+skv_status launch_contiguous(const int64_t* costs, int n, int P, int J, int32_t* roc, int32_t* order,
+                             int64_t* load, const skv_host::Ctx& c);
+skv_status launch_zigzag(const skv_problem& pb, const int32_t* st, const int32_t* len, int n_samples,
+                         int64_t* load, const skv_host::Ctx& c);
+skv_status launch_rank_csr(const int32_t* roc, int n, int P, int32_t* ptr, int32_t* list,
+                           const skv_host::Ctx& c);
+
+skv_status launch_merge(const float* o_part, const float* lse_part, int P, int64_t rows, int d,
+                        void* o, skv_dtype o_dtype, float* lse, const skv_host::Ctx& c);
+// D_r = dO_r . o_r and lse2_r = lse_r * log2(e) (base-2 LSE for exp2 kernels)
+skv_status launch_bwd_prep(const void* o, const void* dO, const float* lse, skv_dtype dt, int64_t rows,
+                           int d, float* D, float* lse2, const skv_host::Ctx& c);
+// dq[r] = sum_p dq_part[p][r]
+skv_status launch_dq_sum(const float* dq_part, int P, int64_t rows, int d, float* dq,
+                         const skv_host::Ctx& c);
+skv_status launch_zero(float* p, int64_t n, const skv_host::Ctx& c);
+
+// fp32 CUDA-core attention (any dtype input), one CTA per (block, head, rank)
+skv_status launch_attn_fwd_simt(const skv_problem& pb, const void* q, const void* k, const void* v,
+                                skv::RankCSR csr, float* o_part, float* lse_part, const skv_host::Ctx& c);
+skv_status launch_attn_bwd_simt(const skv_problem& pb, const void* q, const void* k, const void* v,
+                                const void* dO, const float* lse, const float* D, skv::RankCSR csr,
+                                float* dq_part, float* dk, float* dv, const skv_host::Ctx& c);
+
+}  // namespace skv_internal

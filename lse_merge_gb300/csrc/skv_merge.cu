@@ -1,0 +1,228 @@
+// Bandwidth-bound passes of libskv: the exact LSE merge of per-rank partials
+// [Split-KV §4.1, Eq. 4; Alg. 1 line 8], the backward pre-pass
+// D_r = dO_r . o_r (Alg. 1 line 15, merged form) and the dq sum over ranks
+// (Alg. 1 line 17 made local).  "Split-KV: Efficient Context Parallelism for
+// Training Diffusion Drafters".
+//
+// The merge is one HBM pass: G = d/4 lanes own one row (16-byte vectors, rows
+// of 64 or 128 floats are one or half a warp); the row's P log-sum-exps are
+// loaded one per lane, reduced with warp shuffles, and only partials with a
+// finite l_p are read -- so the bytes moved are the algorithmic ones.
+#include <math.h>
+
+#include "skv_common.cuh"
+#include "skv_internal.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void store4(float* dst, float4 v) { __stcs(reinterpret_cast<float4*>(dst), v); }
+__device__ __forceinline__ void store4(__nv_bfloat16* dst, float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst) = u;
+}
+
+// G lanes per row (G divides 32); each lane owns VPL float4 columns.
+template <int G, int VPL, typename OT>
+__global__ void __launch_bounds__(kThreads)
+lse_merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int P,
+                 int64_t rows, OT* __restrict__ o, float* __restrict__ lse_out) {
+    constexpr int D4 = G * VPL;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % G;                  // lane inside the row group
+    const int grp = lane / G;                  // row group inside the warp
+    constexpr int kRowsPerWarp = 32 / G;
+    constexpr unsigned kGroupBits = (G >= 32) ? 0xffffffffu : ((1u << (G & 31)) - 1u);
+    const unsigned gmask = (G >= 32) ? 0xffffffffu : (kGroupBits << (grp * G));
+    const int64_t warp_global = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t r0 = warp_global * kRowsPerWarp; r0 < rows; r0 += n_warps * kRowsPerWarp) {
+        const int64_t r = r0 + grp;
+        const bool live = r < rows;
+        // pass 1: max and sum of exp over the row's partials (lanes stride over p)
+        float mx = -INFINITY;
+        for (int p = sub; p < P; p += G) {
+            const float l = live ? __ldcs(lse_part + int64_t(p) * rows + r) : -INFINITY;
+            mx = fmaxf(mx, l);
+        }
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(gmask, mx, off));
+        float den = 0.f;
+        if (mx != -INFINITY) {
+            for (int p = sub; p < P; p += G) {
+                const float l = __ldcs(lse_part + int64_t(p) * rows + r);
+                den += (l == -INFINITY) ? 0.f : __expf(l - mx);
+            }
+        }
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) den += __shfl_xor_sync(gmask, den, off);
+        const float L = (mx == -INFINITY) ? -INFINITY : mx + __logf(den);
+        // pass 2: o = sum_p exp(l_p - L) o_p over finite partials
+        float4 acc[VPL];
+#pragma unroll
+        for (int t = 0; t < VPL; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live && L != -INFINITY) {
+            for (int pb = 0; pb < P; pb += G) {
+                const int p_me = pb + sub;
+                const float l_me = p_me < P ? __ldcs(lse_part + int64_t(p_me) * rows + r) : -INFINITY;
+                const float w_me = (l_me == -INFINITY) ? 0.f : __expf(l_me - L);
+                unsigned fin = __ballot_sync(gmask, l_me != -INFINITY);
+                if (G < 32) fin = (fin >> (grp * G)) & kGroupBits;
+                // four partials in flight per lane
+                while (fin) {
+                    int ps[4];
+                    float ws[4];
+                    int cnt = 0;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        ps[u] = -1;
+                        ws[u] = 0.f;
+                        if (fin) {
+                            const int b = __ffs(fin) - 1;
+                            fin &= fin - 1;
+                            ps[u] = pb + b;
+                            ws[u] = __shfl_sync(gmask, w_me, grp * G + b);
+                            ++cnt;
+                        } else {
+                            __shfl_sync(gmask, w_me, grp * G);   // keep the group converged
+                        }
+                    }
+                    float4 val[4][VPL];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+                        for (int t = 0; t < VPL; ++t) {
+                            if (ps[u] >= 0) {
+                                const float4* src = reinterpret_cast<const float4*>(
+                                    o_part + (int64_t(ps[u]) * rows + r) * (4 * D4));
+                                val[u][t] = __ldcs(src + sub + t * G);
+                            } else {
+                                val[u][t] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int t = 0; t < VPL; ++t) {
+                            acc[t].x = fmaf(ws[u], val[u][t].x, acc[t].x);
+                            acc[t].y = fmaf(ws[u], val[u][t].y, acc[t].y);
+                            acc[t].z = fmaf(ws[u], val[u][t].z, acc[t].z);
+                            acc[t].w = fmaf(ws[u], val[u][t].w, acc[t].w);
+                        }
+                    (void)cnt;
+                }
+            }
+        }
+        if (live) {
+#pragma unroll
+            for (int t = 0; t < VPL; ++t) store4(o + r * (4 * D4) + 4 * (sub + t * G), acc[t]);
+            if (lse_out && sub == 0) lse_out[r] = L;
+        }
+    }
+}
+
+template <typename OT>
+skv_status merge_dispatch(const float* o_part, const float* lse_part, int P, int64_t rows, int d, OT* o,
+                          float* lse, const skv_host::Ctx& c) {
+    const int64_t warps_needed = rows;   // upper bound
+    int blocks = c.num_sms * 8;
+    const int64_t max_blocks = (warps_needed + (kThreads / 32) - 1) / (kThreads / 32);
+    if (blocks > max_blocks) blocks = (int)(max_blocks > 0 ? max_blocks : 1);
+    switch (d) {
+        case 64:  lse_merge_kernel<16, 1, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
+        case 128: lse_merge_kernel<32, 1, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
+        case 256: lse_merge_kernel<32, 2, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
+        case 32:  lse_merge_kernel<8, 1, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
+        case 16:  lse_merge_kernel<4, 1, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
+        case 8:   lse_merge_kernel<2, 1, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
+        case 4:   lse_merge_kernel<1, 1, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
+        default: return SKV_ERR_UNSUPPORTED;
+    }
+    SKV_LAUNCHED();
+    return SKV_OK;
+}
+
+// D_r = sum_t dO[r,t] * o[r,t] and lse2_r = lse_r * log2(e): one warp per row.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ dO, const float* __restrict__ lse,
+                int64_t rows, int d, float* __restrict__ D, float* __restrict__ lse2) {
+    const int lane = threadIdx.x & 31;
+    const int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t r = w; r < rows; r += nw) {
+        float acc = 0.f;
+        for (int t = lane; t < d; t += 32)
+            acc = fmaf(skv::to_f32(o[r * d + t]), skv::to_f32(dO[r * d + t]), acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) {
+            D[r] = acc;
+            lse2[r] = lse[r] * 1.4426950408889634f;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+dq_sum_kernel(const float4* __restrict__ part, int P, int64_t n4, float4* __restrict__ dq) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
+        float4 acc = __ldcs(part + i);
+        for (int p = 1; p < P; ++p) {
+            const float4 v = __ldcs(part + int64_t(p) * n4 + i);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        __stcs(dq + i, acc);
+    }
+}
+
+}  // namespace
+
+namespace skv_internal {
+
+skv_status launch_merge(const float* o_part, const float* lse_part, int P, int64_t rows, int d, void* o,
+                        skv_dtype o_dtype, float* lse, const skv_host::Ctx& c) {
+    if (rows == 0) return SKV_OK;
+    if (o_dtype == SKV_BF16)
+        return merge_dispatch(o_part, lse_part, P, rows, d, static_cast<__nv_bfloat16*>(o), lse, c);
+    return merge_dispatch(o_part, lse_part, P, rows, d, static_cast<float*>(o), lse, c);
+}
+
+skv_status launch_bwd_prep(const void* o, const void* dO, const float* lse, skv_dtype dt, int64_t rows, int d,
+                           float* D, float* lse2, const skv_host::Ctx& c) {
+    if (rows == 0) return SKV_OK;
+    int64_t blocks = (rows + (kThreads / 32) - 1) / (kThreads / 32);
+    if (blocks > int64_t(c.num_sms) * 8) blocks = int64_t(c.num_sms) * 8;
+    if (dt == SKV_BF16)
+        bwd_prep_kernel<<<(unsigned)blocks, kThreads, 0, c.stream>>>(
+            static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, rows, d, D, lse2);
+    else
+        bwd_prep_kernel<<<(unsigned)blocks, kThreads, 0, c.stream>>>(
+            static_cast<const float*>(o), static_cast<const float*>(dO), lse, rows, d, D, lse2);
+    SKV_LAUNCHED();
+    return SKV_OK;
+}
+
+skv_status launch_dq_sum(const float* dq_part, int P, int64_t rows, int d, float* dq, const skv_host::Ctx& c) {
+    const int64_t n4 = rows * d / 4;
+    if (n4 == 0) return SKV_OK;
+    int64_t blocks = (n4 + kThreads - 1) / kThreads;
+    if (blocks > int64_t(c.num_sms) * 8) blocks = int64_t(c.num_sms) * 8;
+    dq_sum_kernel<<<(unsigned)blocks, kThreads, 0, c.stream>>>(reinterpret_cast<const float4*>(dq_part), P, n4,
+                                                              reinterpret_cast<float4*>(dq));
+    SKV_LAUNCHED();
+    return SKV_OK;
+}
+
+skv_status launch_zero(float* p, int64_t n, const skv_host::Ctx& c) {
+    if (n == 0) return SKV_OK;
+    SKV_CUDA_CHECK(cudaMemsetAsync(p, 0, size_t(n) * sizeof(float), c.stream));
+    return SKV_OK;
+}
+
+}  // namespace skv_internal
