@@ -153,8 +153,11 @@ def run_reference(args):
     if rank != 0:
         return 0
     from workloads import WORKLOADS, make_inputs
+    import torch
     w = WORKLOADS[args.workload]
-    inp = make_inputs(w)
+    # the same draw as our arm (device generator when a GPU is present); the
+    # oracle itself runs on the host cores only
+    inp = make_inputs(w, device="cuda" if torch.cuda.is_available() else "cpu")
     per_step = []
     for t in range(args.warmup + args.steps):
         tf, desc, dt = oracle_sample(w, inp, args.ref_step_s, block_offset=7 * t)
@@ -199,12 +202,12 @@ def run_ours(args):
     w = WORKLOADS[args.workload]
     if world > 1:
         w = w.with_(seed=w.seed + 1000 * rank)     # independent replica per rank
-    inp = make_inputs(w, with_grad=w.backward, pin=True)
     dev = torch.device("cuda", local_rank)
+    inp = make_inputs(w, with_grad=w.backward, device=str(dev))
     tdt = torch.float32 if w.dtype == "fp32" else torch.bfloat16
     s, a = inp.s.to(dev), inp.a.to(dev)
-    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
-    dO = inp.dO.to(dev) if w.backward else None
+    q, k, v = inp.q, inp.k, inp.v
+    dO = inp.dO if w.backward else None
     prob = skv.Problem(s, a, w.B, w.H, w.d, w.S, w.m, w.P, tdt)
     P, Q, H, d = w.P, w.Q, w.H, w.d
     o_part = torch.empty(P, Q, H, d, dtype=torch.float32, device=dev)
@@ -307,7 +310,7 @@ def run_ours(args):
         h_dq = torch.empty(Q, H, d, dtype=torch.float32, pin_memory=True)
         h_dk = torch.empty(w.S, H, d, dtype=torch.float32, pin_memory=True)
         h_dv = torch.empty(w.S, H, d, dtype=torch.float32, pin_memory=True)
-        h_in = [(inp.s, s), (inp.a, a), (inp.q, q), (inp.k, k), (inp.v, v), (inp.dO, dO)]
+        h_in = [(x.cpu().pin_memory(), x) for x in (s, a, q, k, v, dO)]
         h_out = [(o, h_o), (lse, h_lse), (dq, h_dq), (dk, h_dk), (dv, h_dv)]
         bi = sum(x.numel() * x.element_size() for x, _ in h_in)
         bo = sum(x.numel() * x.element_size() for x, _ in h_out)

@@ -1,0 +1,93 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py
+times: the oracle computes sampled outputs one query block / key at a time
+(two heads, 0 and H-1), and properties that hold at any size are checked on
+every output (the exact -inf pattern of the partials, finiteness)."""
+import numpy as np
+import pytest
+import torch
+
+import lse_merge_gb300 as skv
+import oracle as orc
+from gpu_helpers import TOL_BF16, TOL_BF16_LSE, assert_lse_equal, maxabs
+from workloads import LONG_1M, PACKED, make_inputs, qs_sweep
+
+pytestmark = pytest.mark.gpu
+
+FULL = [PACKED, LONG_1M, qs_sweep(4, "contiguous"), qs_sweep(32, "lpt")]
+
+
+def sample_blocks(N, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 7, 8, N // 2, N - 1]
+    return sorted(set(fixed + rng.integers(0, N, size=3).tolist()))
+
+
+def empty_pattern(s, a, roc, m, P, B, H):
+    """Exact -inf pattern of lse_part: row of block i is empty on rank p iff no
+    chunk of p meets [s_i, a_i)."""
+    s = s.numpy().astype(np.int64)
+    a = a.numpy().astype(np.int64)
+    N = len(s)
+    has = np.zeros((P, N), bool)
+    for j, p in enumerate(roc):
+        lo, hi = j * m, (j + 1) * m
+        has[p] |= (np.minimum(a, hi) - np.maximum(s, lo)) > 0
+    return np.repeat(~has, B, axis=1)[:, :, None].repeat(H, axis=2)
+
+
+@pytest.fixture(scope="module", params=FULL, ids=lambda w: w.name)
+def full_run(request):
+    w = request.param
+    inp = make_inputs(w, device="cuda")
+    s, a = inp.s.cuda(), inp.a.cuda()
+    prob = skv.Problem(s, a, w.B, w.H, w.d, w.S, w.m, w.P, torch.bfloat16)
+    costs, roc, _, _ = skv.plan(prob, w.order)
+    o_part, lse_part = skv.attn_fwd(prob, inp.q, inp.k, inp.v, roc)
+    o, lse = skv.lse_merge(o_part, lse_part, out_dtype=torch.bfloat16)
+    assert skv.stream_status() == 0
+    yield w, inp, prob, roc.cpu().numpy(), o_part, lse_part, o, lse
+    del o_part, lse_part
+    torch.cuda.empty_cache()
+
+
+def test_full_partials_pattern_and_finiteness(full_run):
+    w, inp, prob, roc, o_part, lse_part, o, lse = full_run
+    lp = lse_part.cpu().numpy()
+    assert np.array_equal(np.isneginf(lp), empty_pattern(inp.s, inp.a, roc, w.m, w.P, w.B, w.H))
+    assert not np.isnan(lp).any() and not np.isposinf(lp).any()
+    assert torch.isfinite(o.float()).all()
+    assert torch.isfinite(lse).all()          # every block of these workloads sees some context
+    # merge never lowers the log-sum-exp below a partial
+    assert bool((lse[None] >= lse_part - 1e-4).all())
+
+
+def test_full_merged_sampled_blocks(full_run):
+    w, inp, prob, roc, o_part, lse_part, o, lse = full_run
+    heads = [0, w.H - 1]
+    blocks = sample_blocks(w.N, w.seed)
+    r_o, r_l = orc.attention_forward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, blocks=blocks, heads=heads)
+    rows = np.concatenate([np.arange(i * w.B, (i + 1) * w.B) for i in blocks])
+    rt = torch.as_tensor(rows, device="cuda")
+    g_o = o[rt][:, heads].float().cpu().numpy()
+    g_l = lse[rt][:, heads].cpu().numpy()
+    assert_lse_equal(g_l, r_l[rows][:, heads], TOL_BF16_LSE)
+    err = maxabs(g_o, r_o[rows][:, heads])
+    assert err <= TOL_BF16, err
+
+
+def test_full_partials_sampled_ranks(full_run):
+    w, inp, prob, roc, o_part, lse_part, o, lse = full_run
+    heads = [0, w.H - 1]
+    blocks = sample_blocks(w.N, w.seed + 1)[:4]
+    rows = np.concatenate([np.arange(i * w.B, (i + 1) * w.B) for i in blocks])
+    lp = lse_part.cpu().numpy()
+    # the two ranks with the most finite partials among the sampled rows
+    fin = np.isfinite(lp[:, rows][:, :, heads]).sum(axis=(1, 2))
+    for p in np.argsort(-fin)[:2]:
+        km = orc.chunk_key_mask(roc, int(p), w.m, w.S)
+        r_o, r_l = orc.attention_forward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, key_mask=km, blocks=blocks,
+                                         heads=heads)
+        assert_lse_equal(lp[p][rows][:, heads], r_l[rows][:, heads], TOL_BF16_LSE)
+        g = o_part[int(p)][torch.as_tensor(rows, device="cuda")][:, heads].cpu().numpy()
+        mask = np.isfinite(r_l[rows][:, heads])[..., None].repeat(w.d, axis=-1)
+        assert maxabs(g, r_o[rows][:, heads], mask) <= TOL_BF16

@@ -129,21 +129,33 @@ class Inputs:
     dO: Optional[torch.Tensor]  # [Q, H, d] or None
 
 
-def make_inputs(w: Workload, with_grad: Optional[bool] = None, pin: bool = False) -> Inputs:
-    """Draws one workload's inputs on the host.  bf16 workloads round the fp32
-    draws to bf16 (round to nearest even); the oracle widens exactly those
-    values to fp64."""
+def make_inputs(w: Workload, with_grad: Optional[bool] = None, pin: bool = False,
+                device: str = "cpu") -> Inputs:
+    """Draws one workload's inputs.  bf16 workloads round the fp32 draws to
+    bf16 (round to nearest even); the oracle widens exactly those values to
+    fp64.  Anchors always come from the seeded CPU generator; q, k, v, dO come
+    from a generator on ``device`` ("cpu", or "cuda" for the large workloads,
+    whose host draw would take minutes) -- both sides of a parity check read
+    the same tensors, so the device only changes which values are drawn."""
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed)
     s, a = draw_anchors(w, g)
     tdt = torch.float32 if w.dtype == "fp32" else torch.bfloat16
+    if device != "cpu":
+        g = torch.Generator(device=device)
+        g.manual_seed(w.seed)
 
     def draw(shape, std):
-        x = torch.randn(shape, generator=g, dtype=torch.float32)
-        if std != 1.0:
-            x.mul_(std)
-        x = x.to(tdt)
-        return x.pin_memory() if pin else x
+        out = torch.empty(shape, dtype=tdt, device=device)
+        flat = out.view(-1)
+        step = 1 << 26                      # bounded fp32 temporaries
+        for i in range(0, flat.numel(), step):
+            n = min(step, flat.numel() - i)
+            x = torch.randn(n, generator=g, dtype=torch.float32, device=device)
+            if std != 1.0:
+                x.mul_(std)
+            flat[i:i + n] = x.to(tdt)
+        return out.pin_memory() if (pin and device == "cpu") else out
 
     q = draw((w.Q, w.H, w.d), w.qkv_std)
     k = draw((w.S, w.H, w.d), w.qkv_std)
