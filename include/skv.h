@@ -207,10 +207,11 @@ SKV_API skv_status skv_stream_status(void* stream);
 SKV_API const char* skv_status_str(skv_status status);
 
 /*
- * Test hook: iteration cap of every bounded on-device wait of the tensor-core
- * kernels on the current device (default 2^31).  A wait that runs out sets
- * SKV_ERR_TIMEOUT, abandons the work item and lets the kernel finish cleanly.
- * `limit` <= 0 restores the default.
+ * Test hook: time limit in nanoseconds (device global timer) of every bounded
+ * on-device wait of the tensor-core kernels launched afterwards by this
+ * process (default 2 s).  A wait that runs out sets SKV_ERR_TIMEOUT in the
+ * device status word, abandons the work item and lets the kernel finish
+ * cleanly.  `limit` <= 0 restores the default.
  */
 SKV_API skv_status skv_set_wait_limit(int64_t limit);
 

@@ -125,7 +125,7 @@ skv_status get_ctx(void* stream, Ctx& ctx) {
         }
         ctx.status = g_status_ptr[dev];
         ctx.num_sms = g_num_sms[dev];
-        ctx.wait_limit = g_wait_limit > 0 ? g_wait_limit : (1LL << 31);
+        ctx.wait_limit = g_wait_limit > 0 ? g_wait_limit : 2000000000LL;   // ns
     }
     ctx.stream = static_cast<cudaStream_t>(stream);
     return SKV_OK;

@@ -32,7 +32,7 @@ constexpr int BM = 128;          // query rows per tile
 constexpr int BN = 128;          // keys per tile
 constexpr int kStages = 2;
 constexpr int kFwdThreads = 192;
-constexpr long long kTeardownWait = 1LL << 30;
+constexpr long long kTeardownWait = 2000000000LL;   // ns; in-flight copies / MMAs end in microseconds
 
 template <int D>
 struct __align__(1024) FwdSmem {
@@ -205,6 +205,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 while (cnt.next(x0)) ++T;
             }
             bool ok = true;
+            bool issued = false;   // any MMA in flight to wait for before TMEM is freed
             auto fail = [&]() {
                 atomicExch(&sm.abort_flag, 1);
                 skv::raise_status(status, SKV_ERR_TIMEOUT);
@@ -222,6 +223,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     const uint64_t bd = smem_desc(smem_u32(sm.k[st][kk >> 2]) + off, 16, 1024);
                     mma_ss(dS, ad, bd, idS, kk > 0);
                 }
+                issued = true;
                 mma_commit(&sm.s_full[n & 1]);
             };
             if (T > 0) {
@@ -243,16 +245,23 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                         const uint64_t bd = smem_desc(smem_u32(sm.v[st][0]) + kk * 2048, BN * 128, 1024);
                         mma_ts(tO, aP + kk * 8, bd, idO, (n > 0 || kk > 0) ? 1u : 0u);
                     }
+                    issued = true;
                     mma_commit(&sm.o_done[n & 1]);
                     mma_commit(&sm.kv_empty[st]);
                 }
             }
             // all MMAs this thread issued have completed before TMEM is freed
-            mma_commit(&sm.mma_fin);
-            mbar_wait(&sm.mma_fin, 0, kTeardownWait);
+            // (a commit is only made when there is an MMA to track)
+            if (issued) {
+                mma_commit(&sm.mma_fin);
+                if (!mbar_wait(&sm.mma_fin, 0, kTeardownWait)) skv::raise_status(status, SKV_ERR_TIMEOUT);
+            }
         }
     } else {
         // ------------------------------------------------------------ softmax
+        // tcgen05.ld/st are warp-collective: every branch around them is made
+        // warp-uniform (__any_sync / __all_sync); per-row choices are data.
+        constexpr unsigned kAll = 0xffffffffu;
         const int r = tid;                         // row inside the tile == TMEM lane
         const int64_t row = int64_t(qt) * BM + r;
         const bool live = row < Qn;
@@ -262,11 +271,17 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         float m_ref = -INFINITY, l = 0.f;
         int o_waited = 0;
         bool ok = true;
+        auto uniform_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+            const bool got = __all_sync(kAll, mbar_wait(bar, parity, wait_limit));
+            if (!got && lane == 0) {
+                atomicExch(&sm.abort_flag, 1);
+                skv::raise_status(status, SKV_ERR_TIMEOUT);
+            }
+            return got;
+        };
         auto wait_o = [&](int need) {
             while (ok && o_waited < need) {
-                if (!mbar_wait(&sm.o_done[o_waited & 1], (o_waited >> 1) & 1, wait_limit)) {
-                    atomicExch(&sm.abort_flag, 1);
-                    skv::raise_status(status, SKV_ERR_TIMEOUT);
+                if (!uniform_wait(&sm.o_done[o_waited & 1], (o_waited >> 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -276,13 +291,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         int64_t x0;
         int n = 0;
         while (ok && it.next(x0)) {
-            if (*(volatile int*)&sm.abort_flag) { ok = false; break; }
-            if (!mbar_wait(&sm.s_full[n & 1], (n >> 1) & 1, wait_limit)) {
-                atomicExch(&sm.abort_flag, 1);
-                skv::raise_status(status, SKV_ERR_TIMEOUT);
-                ok = false;
-                break;
-            }
+            if (__any_sync(kAll, *(volatile int*)&sm.abort_flag != 0)) { ok = false; break; }
+            if (!uniform_wait(&sm.s_full[n & 1], (n >> 1) & 1)) { ok = false; break; }
             tc_fence_after();
             float sc[BN];
 #pragma unroll
@@ -312,10 +322,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 rescale = (l > 0.f);
                 m_ref = mx_s;
             }
+            const bool warp_rescale = __any_sync(kAll, rescale);
             // P buffer n&1 was last read by PV_{n-2}; O must be final before a rescale
-            wait_o(rescale ? n : n - 1);
+            wait_o(warp_rescale ? n : n - 1);
             if (!ok) break;
-            if (rescale) {
+            if (warp_rescale) {
+                const float f = rescale ? alpha : 1.f;
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -323,7 +335,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     tmem_ld32(tO + lane_base + c * 32, rr);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * alpha);
+                    for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
                     tmem_st32(tO + lane_base + c * 32, rr);
                 }
             }
@@ -350,26 +362,32 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             ++n;
         }
         wait_o(n);
-        if (ok && !*(volatile int*)&sm.abort_flag && live) {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+        const bool aborted = __any_sync(kAll, *(volatile int*)&sm.abort_flag != 0);
+        if (ok && !aborted) {
+            const bool mine = live && l > 0.f;
+            const float inv = mine ? 1.f / l : 0.f;
             float* dst = o_part + ((int64_t(p) * Qn + row) * H + h) * D;
-            if (n > 0 && l > 0.f) {
+            if (n > 0 && __any_sync(kAll, mine)) {
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t rr[32];
                     tmem_ld32(tO + lane_base + c * 32, rr);
                     tmem_ld_wait();
+                    if (mine) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        float4 v4 = make_float4(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv,
-                                                __uint_as_float(rr[j + 2]) * inv, __uint_as_float(rr[j + 3]) * inv);
-                        __stcs(reinterpret_cast<float4*>(dst + c * 32 + j), v4);
+                        for (int j = 0; j < 32; j += 4) {
+                            float4 v4 = make_float4(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv,
+                                                    __uint_as_float(rr[j + 2]) * inv,
+                                                    __uint_as_float(rr[j + 3]) * inv);
+                            __stcs(reinterpret_cast<float4*>(dst + c * 32 + j), v4);
+                        }
                     }
                 }
             }
-            lse_part[(int64_t(p) * Qn + row) * H + h] =
-                (l > 0.f) ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            if (live)
+                lse_part[(int64_t(p) * Qn + row) * H + h] =
+                    mine ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
     }
     tc_fence_before();

@@ -44,12 +44,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete; false when
-// `limit` polls ran out (the caller records a timeout and abandons its work).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit) {
-    for (long long i = 0; i < limit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase with the given parity to complete: gives up
+// after `limit_ns` nanoseconds of the global timer and returns false (the
+// caller records a timeout and abandons its work).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (static_cast<long long>(global_timer_ns() - t0) > limit_ns) return false;
+    }
 }
 
 // --------------------------------------------------------------------- TMA

@@ -116,3 +116,4 @@ def test_merge_random_partials():
             assert np.all(np.isfinite(got))
             assert np.all(got[:3] == 0)
             assert maxabs(got, r_o) <= tol * max(1.0, float(np.abs(r_o).max()))
+
