@@ -122,7 +122,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     constexpr int NP = D / 64;                       // 64-column panels per row
     constexpr uint32_t kTileBytes = BN * D * 2;      // one K or V tile (== Q tile)
 
-    const TileBounds tb = tile_bounds(s, a, B, Qn, S, qt);
+    TileBounds tb = tile_bounds(s, a, B, Qn, S, qt);
+    // once any block of the launch has timed out the result is void: the
+    // remaining blocks skip their work instead of each waiting out a deadline
+    if (*(volatile int*)status == SKV_ERR_TIMEOUT) tb.hi = tb.lo;
 
     if (tid == 0) {
         mbar_init(&sm.q_full, 1);
