@@ -244,18 +244,25 @@ skv_status skv_attn_bwd(const skv_problem* pb_in, const void* q, const void* k, 
     skv_host::Ctx c;
     if ((st = skv_host::get_ctx(stream, c)) != SKV_OK) return st;
     const int64_t kv_elems = pb.S * pb.n_heads * pb.head_dim;
-    if ((st = skv_internal::launch_zero(dk, kv_elems, c)) != SKV_OK) return st;
-    if ((st = skv_internal::launch_zero(dv, kv_elems, c)) != SKV_OK) return st;
+    const bool tc = skv_tc::bwd_supported(pb);
+    if (rows == 0 || !tc) {   // the tensor-core kernel writes every dk/dv row itself
+        if ((st = skv_internal::launch_zero(dk, kv_elems, c)) != SKV_OK) return st;
+        if ((st = skv_internal::launch_zero(dv, kv_elems, c)) != SKV_OK) return st;
+    }
     if (rows == 0) return SKV_OK;
     BwdWs w;
     bwd_ws_layout(pb, &w, static_cast<char*>(workspace));
     const int n = (int)(pb.S / pb.m);
-    if ((st = skv_internal::launch_rank_csr(rank_of_chunk, n, pb.P, w.csr_ptr, w.csr_list, c)) != SKV_OK) return st;
     if ((st = skv_internal::launch_bwd_prep(o, dO, lse, pb.dtype, rows, pb.head_dim, w.D, w.lse2, c)) != SKV_OK)
         return st;
+    if (tc) {
+        // key tiles are visited rank by rank inside the kernel's tile lists; dq^(p)
+        // of every rank is summed into dq by fp32 reductions
+        skv::RankCSR none{nullptr, nullptr};
+        return skv_tc::launch_attn_bwd_tc(pb, q, k, v, dO, w.lse2, w.D, none, dq, dk, dv, w.tc, c);
+    }
+    if ((st = skv_internal::launch_rank_csr(rank_of_chunk, n, pb.P, w.csr_ptr, w.csr_list, c)) != SKV_OK) return st;
     skv::RankCSR csr{w.csr_ptr, w.csr_list};
-    if (skv_tc::bwd_supported(pb))
-        return skv_tc::launch_attn_bwd_tc(pb, q, k, v, dO, w.lse2, w.D, csr, dq, dk, dv, w.tc, c);
     if ((st = skv_internal::launch_attn_bwd_simt(pb, q, k, v, dO, lse, w.D, csr, w.dq_part, dk, dv, c)) != SKV_OK)
         return st;
     return skv_internal::launch_dq_sum(w.dq_part, pb.P, rows, pb.head_dim, dq, c);

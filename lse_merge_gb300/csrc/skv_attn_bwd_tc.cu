@@ -1,0 +1,466 @@
+// Tensor-core backward of the anchor attention (tcgen05 + TMEM + TMA), sm_103a.
+//
+// "Split-KV: Efficient Context Parallelism for Training Diffusion Drafters",
+// Alg. 1 lines 15-17 in merged form: with the global log-sum-exp l_r and
+// D_r = dO_r . o_r, every rank's score gradient is dS = P (dP - D) with
+// P = exp(z - l).  Each virtual rank p owns the key tiles of its chunks, so
+// its dk_p / dv_p rows are written by exactly one thread block each, and its
+// dq^(p) contributions are summed into dq by fp32 reduction adds (the
+// reduce-scatter of Alg. 1 line 17 made local).
+//
+// Key-stationary: one thread block owns a 128-key tile and one head and walks
+// the 128-row query tiles whose windows meet the tile (the tile-skip list
+// built by skv_kv_list_kernel; masked-out query tiles are never loaded).  Per
+// query tile t (TMEM lane = key for S^T, dP^T, dV, dK; = query row for dQ):
+//   S^T  = K Q_t^T          (SS)  -> TMEM A [0,128)
+//   dP^T = V dO_t^T         (SS)  -> TMEM B [128,256)
+//   compute warps: P^T = exp2(S^T scale log2e - l2), bf16 P^T -> TMEM A[0,64);
+//                  dS^T = P^T (dP^T - D), bf16 -> shared memory (swizzled)
+//   dV  += P^T dO_t         (TS)  -> TMEM [256, 256+D)
+//   dK  += dS^T Q_t         (SS)  -> TMEM [384, 384+D)
+//   dQ_t = dS K             (SS, dS^T read MN-major) -> TMEM B
+//   compute warps: dq[rows] += scale dQ_t (red.global.add.v4.f32)
+// Roles (192 threads): warps 0-3 compute, warp 4 MMA issuer, warp 5 TMA.
+#include <cuda.h>
+#include <math.h>
+
+#include "skv_ptx.cuh"
+#include "skv_tc.h"
+#include "skv_tc_common.cuh"
+
+namespace {
+
+using namespace skv_ptx;
+using namespace skv_tcc;
+
+constexpr int kBwdThreads = 192;
+constexpr int kSmemMax = 232448;                     // sm_100-family opt-in maximum per block
+constexpr int kHeaderBytes = 3072;
+constexpr long long kTeardownWait = 2000000000LL;    // ns
+
+struct BwdHeader {
+    uint64_t kv_full, qd_full[2], qd_empty[2], s_full, ds_full, dq_full, dq_free, mma_fin, meta_full;
+    uint32_t tmem_base;
+    int abort_flag;
+    float lse2[BM];
+    float Dr[BM];
+    int32_t rlo[BM];
+    int32_t rhi[BM];
+};
+static_assert(sizeof(BwdHeader) <= kHeaderBytes, "header");
+
+template <int D>
+struct BwdTiles {
+    __nv_bfloat16 k[D / 64][BN * 64];
+    __nv_bfloat16 v[D / 64][BN * 64];
+    __nv_bfloat16 q[2][D / 64][BM * 64];
+    __nv_bfloat16 dO[2][D / 64][BM * 64];
+    __nv_bfloat16 ds[2][BN * 64];       // dS^T [key][q], two 64-query panels
+};
+
+__device__ __forceinline__ void red_add4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+
+// ---------------------------------------------------------------- tile lists
+
+// Per query tile: union (lo, hi) and full-visibility (flo, fhi) key bounds.
+__global__ void qtile_bounds_kernel(const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int64_t Qn,
+                                    int64_t S, int n_qt, int4* __restrict__ out) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= n_qt) return;
+    const TileBounds tb = tile_bounds(s, a, B, Qn, S, t);
+    out[t] = make_int4((int)tb.lo, (int)tb.hi, (int)tb.flo, (int)tb.fhi);
+}
+
+// Tile-skip lists: for key tile k, the ascending query tiles whose union window
+// meets [128k, 128k+128).  One warp per key tile; fixed capacity n_qt per list.
+__global__ void kv_list_kernel(const int4* __restrict__ qtb, int n_qt, int n_kv, int32_t* __restrict__ cnt,
+                               int32_t* __restrict__ list) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= n_kv) return;
+    const int64_t x0 = int64_t(warp) * BN, x1 = x0 + BN;
+    int n = 0;
+    int32_t* dst = list + int64_t(warp) * n_qt;
+    for (int base = 0; base < n_qt; base += 32) {
+        const int t = base + lane;
+        bool hit = false;
+        if (t < n_qt) {
+            const int4 b = qtb[t];
+            hit = b.x < b.y && b.x < x1 && b.y > x0;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (hit) dst[n + __popc(m & ((1u << lane) - 1u))] = t;
+        n += __popc(m);
+    }
+    if (lane == 0) cnt[warp] = n;
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                   const float* __restrict__ lse2_g, const float* __restrict__ D_g, const int32_t* __restrict__ s,
+                   const int32_t* __restrict__ a, int B, int64_t Qn, int H, int64_t S, float scale, float scale_log2,
+                   const int4* __restrict__ qtb, const int32_t* __restrict__ kv_cnt,
+                   const int32_t* __restrict__ kv_list, int n_qt, float* __restrict__ dq, float* __restrict__ dk,
+                   float* __restrict__ dv, int* status, long long wait_limit) {
+    extern __shared__ unsigned char smem_raw[];
+    BwdHeader& hd = *reinterpret_cast<BwdHeader*>(smem_raw);
+    const uint32_t base_s = smem_u32(smem_raw);
+    const uint32_t tiles_s = (base_s + kHeaderBytes + 1023u) & ~1023u;
+    BwdTiles<D>& tl = *reinterpret_cast<BwdTiles<D>*>(smem_raw + (tiles_s - base_s));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kt = blockIdx.x, h = blockIdx.y;
+    const int64_t x0 = int64_t(kt) * BN;
+    constexpr int NP = D / 64;
+    constexpr uint32_t kTile = BM * D * 2;
+    // the swizzled tiles must start on a 1024-byte boundary inside the allocation
+    const bool layout_ok = (tiles_s - base_s) + sizeof(BwdTiles<D>) <= (size_t)kSmemMax;
+    int cnt = kv_cnt[kt];
+    if (!layout_ok || *(volatile int*)status == SKV_ERR_TIMEOUT) cnt = 0;
+    if (!layout_ok && tid == 0) skv::raise_status(status, SKV_ERR_UNSUPPORTED);
+    const int32_t* list = kv_list + int64_t(kt) * n_qt;
+
+    if (tid == 0) {
+        mbar_init(&hd.kv_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&hd.qd_full[i], 1);
+            mbar_init(&hd.qd_empty[i], 1);
+        }
+        mbar_init(&hd.s_full, 1);
+        mbar_init(&hd.ds_full, 128);
+        mbar_init(&hd.dq_full, 1);
+        mbar_init(&hd.dq_free, 128);
+        mbar_init(&hd.mma_fin, 1);
+        mbar_init(&hd.meta_full, 128);
+        hd.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(&hd.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = hd.tmem_base;
+    const uint32_t tA = tmem, tB = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+
+    if (warp == 5) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && cnt > 0) {
+            prefetch_tensormap(&map_q);
+            prefetch_tensormap(&map_do);
+            mbar_arrive_expect_tx(&hd.kv_full, 2 * kTile);
+            for (int c = 0; c < NP; ++c) {
+                tma_load_2d(tl.k[c], &map_k, &hd.kv_full, h * D + c * 64, (int)x0);
+                tma_load_2d(tl.v[c], &map_v, &hd.kv_full, h * D + c * 64, (int)x0);
+            }
+            int t = 0;
+            for (; t < cnt; ++t) {
+                const int st = t & 1;
+                if (t >= 2 && !mbar_wait(&hd.qd_empty[st], ((t - 2) >> 1) & 1, wait_limit)) {
+                    atomicExch(&hd.abort_flag, 1);
+                    skv::raise_status(status, SKV_ERR_TIMEOUT);
+                    break;
+                }
+                if (*(volatile int*)&hd.abort_flag) break;
+                const int row = list[t] * BM;
+                mbar_arrive_expect_tx(&hd.qd_full[st], 2 * kTile);
+                for (int c = 0; c < NP; ++c) {
+                    tma_load_2d(tl.q[st][c], &map_q, &hd.qd_full[st], h * D + c * 64, row);
+                    tma_load_2d(tl.dO[st][c], &map_do, &hd.qd_full[st], h * D + c * 64, row);
+                }
+            }
+            mbar_wait(&hd.kv_full, 0, kTeardownWait);
+            for (int st = 0; st < 2 && st < t; ++st) {
+                const int last = st + ((t - 1 - st) >> 1) * 2;
+                mbar_wait(&hd.qd_full[st], (last >> 1) & 1, kTeardownWait);
+            }
+        }
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && cnt > 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(BN, BM, 0, 0);    // M = keys, N = queries, K = d
+            constexpr uint32_t idKV = idesc_bf16_f32(BN, D, 0, 1);    // M = keys, N = d, K = queries
+            constexpr uint32_t idQ = idesc_bf16_f32(BM, D, 1, 1);     // M = queries, N = d, K = keys
+            bool issued = false;
+            auto fail = [&]() {
+                atomicExch(&hd.abort_flag, 1);
+                skv::raise_status(status, SKV_ERR_TIMEOUT);
+            };
+            bool ok = mbar_wait(&hd.kv_full, 0, wait_limit);
+            if (!ok) fail();
+            for (int t = 0; ok && t < cnt; ++t) {
+                const int st = t & 1;
+                if (t > 0 && !mbar_wait(&hd.dq_free, (t - 1) & 1, wait_limit)) { fail(); break; }
+                if (!mbar_wait(&hd.qd_full[st], (t >> 1) & 1, wait_limit)) { fail(); break; }
+                if (*(volatile int*)&hd.abort_flag) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    mma_ss(tA, smem_desc(smem_u32(tl.k[kk >> 2]) + off, 16, 1024),
+                           smem_desc(smem_u32(tl.q[st][kk >> 2]) + off, 16, 1024), idS, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    mma_ss(tB, smem_desc(smem_u32(tl.v[kk >> 2]) + off, 16, 1024),
+                           smem_desc(smem_u32(tl.dO[st][kk >> 2]) + off, 16, 1024), idS, kk > 0);
+                }
+                issued = true;
+                mma_commit(&hd.s_full);
+                if (!mbar_wait(&hd.ds_full, t & 1, wait_limit)) { fail(); break; }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk)      // dV += P^T dO
+                    mma_ts(tdV, tA + kk * 8, smem_desc(smem_u32(tl.dO[st][0]) + kk * 2048, BM * 128, 1024), idKV,
+                           (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk)      // dK += dS^T Q
+                    mma_ss(tdK, smem_desc(smem_u32(tl.ds[kk >> 2]) + (kk & 3) * 32, 16, 1024),
+                           smem_desc(smem_u32(tl.q[st][0]) + kk * 2048, BM * 128, 1024), idKV,
+                           (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)      // dQ = dS K
+                    mma_ss(tB, smem_desc(smem_u32(tl.ds[0]) + kk * 2048, BN * 128, 1024),
+                           smem_desc(smem_u32(tl.k[0]) + kk * 2048, BN * 128, 1024), idQ, kk > 0);
+                mma_commit(&hd.dq_full);
+                mma_commit(&hd.qd_empty[st]);
+            }
+            if (issued) {
+                mma_commit(&hd.mma_fin);
+                if (!mbar_wait(&hd.mma_fin, 0, kTeardownWait)) skv::raise_status(status, SKV_ERR_TIMEOUT);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ compute
+        constexpr unsigned kAll = 0xffffffffu;
+        const uint32_t lane_base = uint32_t(warp * 32) << 16;
+        const int64_t x = x0 + tid;                 // key row of this thread (S^T, dP^T, dK, dV)
+        bool ok = true;
+        auto uniform_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+            const bool got = __all_sync(kAll, mbar_wait(bar, parity, wait_limit));
+            if (!got && lane == 0) {
+                atomicExch(&hd.abort_flag, 1);
+                skv::raise_status(status, SKV_ERR_TIMEOUT);
+            }
+            return got;
+        };
+        unsigned char* ds_bytes = reinterpret_cast<unsigned char*>(&tl.ds[0][0]);
+        for (int t = 0; t < cnt; ++t) {
+            const int qt = list[t];
+            const int64_t row0 = int64_t(qt) * BM;
+            // the 128 compute threads share the tile's row data through shared
+            // memory; they sync on mbarriers (bounded waits), never bar.sync:
+            // previous tile's rows are read by everyone once ds_full(t-1) completed
+            if (t > 0 && !uniform_wait(&hd.ds_full, (t - 1) & 1)) { ok = false; break; }
+            {
+                const int64_t r = row0 + tid;
+                if (r < Qn) {
+                    hd.lse2[tid] = lse2_g[r * H + h];
+                    hd.Dr[tid] = D_g[r * H + h];
+                    int64_t lo, hi;
+                    skv::block_window(s, a, (int)(r / B), S, lo, hi);
+                    hd.rlo[tid] = (int32_t)lo;
+                    hd.rhi[tid] = (int32_t)hi;
+                } else {
+                    hd.lse2[tid] = INFINITY;         // rows past the end contribute nothing
+                    hd.Dr[tid] = 0.f;
+                    hd.rlo[tid] = 0;
+                    hd.rhi[tid] = 0;
+                }
+            }
+            mbar_arrive(&hd.meta_full);
+            if (!uniform_wait(&hd.meta_full, t & 1)) { ok = false; break; }
+            const int4 b = qtb[qt];
+            const bool full = (x0 >= b.z) && (x0 + BN <= b.w);
+            if (__any_sync(kAll, *(volatile int*)&hd.abort_flag != 0)) { ok = false; break; }
+            if (!uniform_wait(&hd.s_full, t & 1)) { ok = false; break; }
+            tc_fence_after();
+            // 32 query columns at a time: P^T (fp32 in registers, bf16 to TMEM A),
+            // then dS^T from the matching dP^T columns (bf16 to shared memory)
+#pragma unroll 1
+            for (int c = 0; c < BM / 32; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(tA + lane_base + c * 32, rr);
+                tmem_ld_wait();
+                float pr[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int col = c * 32 + j;
+                    float pv = ex2(fmaf(__uint_as_float(rr[j]), scale_log2, -hd.lse2[col]));
+                    if (!full && !(hd.rlo[col] <= x && x < hd.rhi[col])) pv = 0.f;
+                    pr[j] = pv;
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(pr[2 * j], pr[2 * j + 1]);
+                // P^T columns [32c, 32c+32) -> bf16 pairs in TMEM columns [16c, 16c+16); S^T
+                // columns < 32(c+1) have been read already, so the store cannot clobber unread S
+                tmem_st16(tA + lane_base + c * 16, pk);
+                tmem_ld32(tB + lane_base + c * 32, rr);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int c0 = c * 32 + 2 * j;
+                    const float d0 = pr[2 * j] * (__uint_as_float(rr[2 * j]) - hd.Dr[c0]);
+                    const float d1 = pr[2 * j + 1] * (__uint_as_float(rr[2 * j + 1]) - hd.Dr[c0 + 1]);
+                    pk[j] = pack_bf16(d0, d1);
+                }
+                // columns [32c, 32c+32) = panel c/2, 16-byte chunks (c%2)*4 .. +3
+                unsigned char* rowp = ds_bytes + (c >> 1) * (BN * 128) + tid * 128;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int chunk = (c & 1) * 4 + u;
+                    *reinterpret_cast<uint4*>(rowp + ((chunk ^ (tid & 7)) << 4)) =
+                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&hd.ds_full);
+            if (!uniform_wait(&hd.dq_full, t & 1)) { ok = false; break; }
+            tc_fence_after();
+            {
+                const int64_t qrow = row0 + tid;         // TMEM lane = query row for dQ
+                float* dst = dq + (qrow * H + h) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(tB + lane_base + c * 32, rr);
+                    tmem_ld_wait();
+                    if (qrow < Qn) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            red_add4(dst + c * 32 + j, scale * __uint_as_float(rr[j]),
+                                     scale * __uint_as_float(rr[j + 1]), scale * __uint_as_float(rr[j + 2]),
+                                     scale * __uint_as_float(rr[j + 3]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&hd.dq_free);
+        }
+        // dK, dV rows of this key tile (zeros when no query sees it)
+        const bool aborted = __any_sync(kAll, *(volatile int*)&hd.abort_flag != 0);
+        if (!aborted && layout_ok) {
+            float* dkr = dk + (x * H + h) * D;
+            float* dvr = dv + (x * H + h) * D;
+            if (cnt > 0 && ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t rk[32], rv[32];
+                    tmem_ld32(tdK + lane_base + c * 32, rk);
+                    tmem_ld32(tdV + lane_base + c * 32, rv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        __stcs(reinterpret_cast<float4*>(dkr + c * 32 + j),
+                               make_float4(scale * __uint_as_float(rk[j]), scale * __uint_as_float(rk[j + 1]),
+                                           scale * __uint_as_float(rk[j + 2]), scale * __uint_as_float(rk[j + 3])));
+                        __stcs(reinterpret_cast<float4*>(dvr + c * 32 + j),
+                               make_float4(__uint_as_float(rv[j]), __uint_as_float(rv[j + 1]),
+                                           __uint_as_float(rv[j + 2]), __uint_as_float(rv[j + 3])));
+                    }
+                }
+            } else if (cnt == 0) {
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < D; j += 4) {
+                    __stcs(reinterpret_cast<float4*>(dkr + j), z);
+                    __stcs(reinterpret_cast<float4*>(dvr + j), z);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+struct BwdScratch {
+    int4* qtb;
+    int32_t* cnt;
+    int32_t* list;
+};
+
+size_t scratch_layout(const skv_problem& pb, BwdScratch* w, char* base) {
+    using skv_host::align256;
+    const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
+    const int64_t n_qt = (Qn + BM - 1) / BM;
+    const int64_t n_kv = pb.S / BN;
+    size_t off = 0;
+    const size_t o_qtb = off; off = align256(off + size_t(n_qt) * sizeof(int4));
+    const size_t o_cnt = off; off = align256(off + size_t(n_kv) * 4);
+    const size_t o_list = off; off = align256(off + size_t(n_kv) * size_t(n_qt) * 4);
+    if (w) {
+        w->qtb = reinterpret_cast<int4*>(base + o_qtb);
+        w->cnt = reinterpret_cast<int32_t*>(base + o_cnt);
+        w->list = reinterpret_cast<int32_t*>(base + o_list);
+    }
+    return off;
+}
+
+template <int D>
+skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const void* v, const void* dO,
+                      const float* lse2, const float* Dv, float* dq, float* dk, float* dv, void* scratch,
+                      const skv_host::Ctx& c) {
+    const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
+    const int n_qt = (int)((Qn + BM - 1) / BM);
+    const int n_kv = (int)(pb.S / BN);
+    BwdScratch w;
+    scratch_layout(pb, &w, static_cast<char*>(scratch));
+    qtile_bounds_kernel<<<(n_qt + 127) / 128, 128, 0, c.stream>>>(pb.s, pb.a, pb.B, Qn, pb.S, n_qt, w.qtb);
+    SKV_LAUNCHED();
+    kv_list_kernel<<<(n_kv + 7) / 8, 256, 0, c.stream>>>(w.qtb, n_qt, n_kv, w.cnt, w.list);
+    SKV_LAUNCHED();
+    CUtensorMap mq, mdo, mk, mv;
+    const int64_t cols = int64_t(pb.n_heads) * D;
+    if (!make_map(&mq, q, Qn, cols) || !make_map(&mdo, dO, Qn, cols) || !make_map(&mk, k, pb.S, cols) ||
+        !make_map(&mv, v, pb.S, cols))
+        return SKV_ERR_CUDA;
+    SKV_CUDA_CHECK(cudaMemsetAsync(dq, 0, size_t(Qn) * cols * sizeof(float), c.stream));
+    auto kern = attn_bwd_tc_kernel<D>;
+    SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax));
+    const dim3 grid((unsigned)n_kv, (unsigned)pb.n_heads);
+    kern<<<grid, kBwdThreads, kSmemMax, c.stream>>>(mq, mdo, mk, mv, lse2, Dv, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S,
+                                                    pb.scale, pb.scale * 1.4426950408889634f, w.qtb, w.cnt, w.list,
+                                                    n_qt, dq, dk, dv, c.status, c.wait_limit);
+    SKV_LAUNCHED();
+    return SKV_OK;
+}
+
+}  // namespace
+
+namespace skv_tc {
+
+bool bwd_supported(const skv_problem& pb) {
+    return pb.dtype == SKV_BF16 && (pb.head_dim == 64 || pb.head_dim == 128) && pb.m % BN == 0 &&
+           pb.n_heads <= 65535;
+}
+
+size_t bwd_scratch_bytes(const skv_problem& pb) {
+    return bwd_supported(pb) ? scratch_layout(pb, nullptr, nullptr) : 0;
+}
+
+skv_status launch_attn_bwd_tc(const skv_problem& pb, const void* q, const void* k, const void* v, const void* dO,
+                              const float* lse2, const float* D, skv::RankCSR, float* dq, float* dk, float* dv,
+                              void* scratch, const skv_host::Ctx& c) {
+    if (pb.head_dim == 128) return launch_bwd<128>(pb, q, k, v, dO, lse2, D, dq, dk, dv, scratch, c);
+    return launch_bwd<64>(pb, q, k, v, dO, lse2, D, dq, dk, dv, scratch, c);
+}
+
+}  // namespace skv_tc

@@ -23,13 +23,13 @@
 
 #include "skv_ptx.cuh"
 #include "skv_tc.h"
+#include "skv_tc_common.cuh"
 
 namespace {
 
 using namespace skv_ptx;
+using namespace skv_tcc;
 
-constexpr int BM = 128;          // query rows per tile
-constexpr int BN = 128;          // keys per tile
 constexpr int kStages = 2;
 constexpr int kFwdThreads = 192;
 constexpr long long kTeardownWait = 2000000000LL;   // ns; in-flight copies / MMAs end in microseconds
@@ -46,34 +46,6 @@ struct __align__(1024) FwdSmem {
     uint32_t tmem_base;
     int abort_flag;
 };
-
-// Rows [qt*128, qt*128+128) of the packed query: tile-level key bounds.
-struct TileBounds {
-    int64_t lo, hi;     // union of the rows' windows (empty if lo >= hi)
-    int64_t flo, fhi;   // intersection: keys every live row sees
-};
-
-__device__ __forceinline__ TileBounds tile_bounds(const int32_t* s, const int32_t* a, int B, int64_t Qn, int64_t S,
-                                                  int qt) {
-    TileBounds tb{S, 0, 0, S};
-    const int64_t r0 = int64_t(qt) * BM;
-    const int64_t r1 = (r0 + BM < Qn ? r0 + BM : Qn) - 1;
-    bool any_empty = false;
-    for (int64_t i = r0 / B; i <= r1 / B; ++i) {
-        int64_t lo, hi;
-        skv::block_window(s, a, (int)i, S, lo, hi);
-        if (hi > lo) {
-            tb.lo = lo < tb.lo ? lo : tb.lo;
-            tb.hi = hi > tb.hi ? hi : tb.hi;
-        } else {
-            any_empty = true;
-        }
-        tb.flo = lo > tb.flo ? lo : tb.flo;
-        tb.fhi = hi < tb.fhi ? hi : tb.fhi;
-    }
-    if (any_empty || r1 - r0 + 1 < BM) tb.fhi = tb.flo;   // partial or empty rows: mask every tile
-    return tb;
-}
 
 // Walks the 128-key tiles of rank p's chunks that intersect [lo, hi).  Every
 // role runs its own copy and sees the same sequence.
@@ -401,32 +373,6 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// 2D bf16 view [rows][cols] of a row-major tensor, 64x128 boxes, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols) {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, 128};
-    cuuint32_t es[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 skv_status launch_fwd(const skv_problem& pb, const void* q, const void* k, const void* v, skv::RankCSR csr,
                       float* o_part, float* lse_part, const skv_host::Ctx& c) {
@@ -455,20 +401,12 @@ bool fwd_supported(const skv_problem& pb) {
     return pb.dtype == SKV_BF16 && (pb.head_dim == 64 || pb.head_dim == 128) && pb.m % BN == 0 &&
            pb.P <= 65535 && pb.n_heads <= 65535;
 }
-bool bwd_supported(const skv_problem&) { return false; }
 size_t fwd_scratch_bytes(const skv_problem&) { return 0; }
-size_t bwd_scratch_bytes(const skv_problem&) { return 0; }
 
 skv_status launch_attn_fwd_tc(const skv_problem& pb, const void* q, const void* k, const void* v, skv::RankCSR csr,
                               float* o_part, float* lse_part, void*, const skv_host::Ctx& c) {
     if (pb.head_dim == 128) return launch_fwd<128>(pb, q, k, v, csr, o_part, lse_part, c);
     return launch_fwd<64>(pb, q, k, v, csr, o_part, lse_part, c);
-}
-
-skv_status launch_attn_bwd_tc(const skv_problem&, const void*, const void*, const void*, const void*,
-                              const float*, const float*, skv::RankCSR, float*, float*, float*, void*,
-                              const skv_host::Ctx&) {
-    return SKV_ERR_UNSUPPORTED;
 }
 
 }  // namespace skv_tc

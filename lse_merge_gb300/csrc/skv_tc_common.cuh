@@ -1,0 +1,70 @@
+// Helpers shared by the tensor-core attention kernels (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "skv_common.cuh"
+
+namespace skv_tcc {
+
+constexpr int BM = 128;          // query rows per tile
+constexpr int BN = 128;          // keys per tile
+
+// Rows [qt*128, qt*128+128) of the packed query: tile-level key bounds.
+struct TileBounds {
+    int64_t lo, hi;     // union of the rows' windows (empty if lo >= hi)
+    int64_t flo, fhi;   // intersection: keys every live row sees
+};
+
+__device__ __forceinline__ TileBounds tile_bounds(const int32_t* s, const int32_t* a, int B, int64_t Qn, int64_t S,
+                                                  int qt) {
+    TileBounds tb{S, 0, 0, S};
+    const int64_t r0 = int64_t(qt) * BM;
+    const int64_t r1 = (r0 + BM < Qn ? r0 + BM : Qn) - 1;
+    bool any_empty = false;
+    for (int64_t i = r0 / B; i <= r1 / B; ++i) {
+        int64_t lo, hi;
+        skv::block_window(s, a, (int)i, S, lo, hi);
+        if (hi > lo) {
+            tb.lo = lo < tb.lo ? lo : tb.lo;
+            tb.hi = hi > tb.hi ? hi : tb.hi;
+        } else {
+            any_empty = true;
+        }
+        tb.flo = lo > tb.flo ? lo : tb.flo;
+        tb.fhi = hi < tb.fhi ? hi : tb.fhi;
+    }
+    if (any_empty || r1 - r0 + 1 < BM) tb.fhi = tb.flo;   // partial or empty rows: mask every tile
+    return tb;
+}
+
+
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2D bf16 view [rows][cols] of a row-major tensor, 64x128 boxes, 128-byte swizzle.
+inline bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+
+}  // namespace skv_tcc

@@ -24,9 +24,9 @@ def dev_inputs(w: Workload, with_grad=None):
 def maxabs(a, b, mask=None):
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)
-    diff = np.abs(a - b)
     if mask is not None:
-        diff = diff[mask]
+        a, b = a[mask], b[mask]
+    diff = np.abs(a - b)
     return float(diff.max()) if diff.size else 0.0
 
 

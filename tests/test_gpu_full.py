@@ -44,14 +44,15 @@ def full_run(request):
     costs, roc, _, _ = skv.plan(prob, w.order)
     o_part, lse_part = skv.attn_fwd(prob, inp.q, inp.k, inp.v, roc)
     o, lse = skv.lse_merge(o_part, lse_part, out_dtype=torch.bfloat16)
+    dq, dk, dv = skv.attn_bwd(prob, inp.q, inp.k, inp.v, o, lse, inp.dO, roc)
     assert skv.stream_status() == 0
-    yield w, inp, prob, roc.cpu().numpy(), o_part, lse_part, o, lse
-    del o_part, lse_part
+    yield w, inp, prob, roc.cpu().numpy(), o_part, lse_part, o, lse, dq, dk, dv
+    del o_part, lse_part, dq, dk, dv
     torch.cuda.empty_cache()
 
 
 def test_full_partials_pattern_and_finiteness(full_run):
-    w, inp, prob, roc, o_part, lse_part, o, lse = full_run
+    w, inp, prob, roc, o_part, lse_part, o, lse, _, _, _ = full_run
     lp = lse_part.cpu().numpy()
     assert np.array_equal(np.isneginf(lp), empty_pattern(inp.s, inp.a, roc, w.m, w.P, w.B, w.H))
     assert not np.isnan(lp).any() and not np.isposinf(lp).any()
@@ -62,7 +63,7 @@ def test_full_partials_pattern_and_finiteness(full_run):
 
 
 def test_full_merged_sampled_blocks(full_run):
-    w, inp, prob, roc, o_part, lse_part, o, lse = full_run
+    w, inp, prob, roc, o_part, lse_part, o, lse, _, _, _ = full_run
     heads = [0, w.H - 1]
     blocks = sample_blocks(w.N, w.seed)
     r_o, r_l = orc.attention_forward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, blocks=blocks, heads=heads)
@@ -76,7 +77,7 @@ def test_full_merged_sampled_blocks(full_run):
 
 
 def test_full_partials_sampled_ranks(full_run):
-    w, inp, prob, roc, o_part, lse_part, o, lse = full_run
+    w, inp, prob, roc, o_part, lse_part, o, lse, _, _, _ = full_run
     heads = [0, w.H - 1]
     blocks = sample_blocks(w.N, w.seed + 1)[:4]
     rows = np.concatenate([np.arange(i * w.B, (i + 1) * w.B) for i in blocks])
@@ -91,3 +92,56 @@ def test_full_partials_sampled_ranks(full_run):
         g = o_part[int(p)][torch.as_tensor(rows, device="cuda")][:, heads].cpu().numpy()
         mask = np.isfinite(r_l[rows][:, heads])[..., None].repeat(w.d, axis=-1)
         assert maxabs(g, r_o[rows][:, heads], mask) <= TOL_BF16
+
+
+def few_attender_keys(s, a, limit=12):
+    """Keys seen by at most `limit` blocks (cheap for the oracle), plus one key
+    past every window of its sample."""
+    s = s.numpy().astype(np.int64)
+    a = a.numpy().astype(np.int64)
+    keys = []
+    for st in np.unique(s)[:2]:
+        aa = np.sort(a[s == st])
+        if len(aa) > limit:
+            keys += [int(aa[-limit]), int(aa[-limit // 2]) + 1, int(aa[-1]) - 1]
+        keys.append(int(aa[-1]) + 3)
+    return sorted(set(k for k in keys if 0 <= k))
+
+
+def test_full_dq_sampled_blocks(full_run):
+    w, inp, prob, _, _, _, _, _, dq, dk, dv = full_run
+    heads = [0, w.H - 1]
+    blocks = sample_blocks(w.N, w.seed + 2)[:5]
+    r_dq, _, _ = orc.attention_backward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, inp.dO, blocks=blocks, heads=heads)
+    rows = np.concatenate([np.arange(i * w.B, (i + 1) * w.B) for i in blocks])
+    g = dq[torch.as_tensor(rows, device="cuda")][:, heads].cpu().numpy()
+    assert maxabs(g, r_dq[rows][:, heads]) <= TOL_BF16
+
+
+def test_full_dkdv_sampled_keys(full_run):
+    w, inp, prob, _, _, _, _, _, dq, dk, dv = full_run
+    heads = [0, w.H - 1]
+    keys = [k for k in few_attender_keys(inp.s, inp.a) if k < w.S]
+    r_dk, r_dv = orc.backward_key_rows(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, inp.dO, keys, heads)
+    kt = torch.as_tensor(keys, device="cuda")
+    assert maxabs(dk[kt][:, heads].cpu().numpy(), r_dk) <= TOL_BF16
+    assert maxabs(dv[kt][:, heads].cpu().numpy(), r_dv) <= TOL_BF16
+
+
+def test_full_gradient_properties(full_run):
+    w, inp, prob, _, _, _, _, _, dq, dk, dv = full_run
+    for t in (dq, dk, dv):
+        assert bool(torch.isfinite(t).all())
+    # keys no window covers get exactly zero gradient
+    seen = torch.zeros(w.S, dtype=torch.bool)
+    for si, ai in zip(inp.s.tolist(), inp.a.tolist()):
+        seen[si:ai] = True
+    unseen = (~seen).nonzero().flatten().cuda()
+    if unseen.numel():
+        assert float(dk[unseen].abs().max()) == 0.0 and float(dv[unseen].abs().max()) == 0.0
+    # softmax rows sum to one: sum_x dv_x = sum_r dO_r (every row sees some key here)
+    for h in (0, w.H - 1):
+        lhs = dv[:, h].double().sum(0)
+        rhs = inp.dO[:, h].double().sum(0)
+        scale = inp.dO[:, h].double().abs().sum(0)
+        assert float(((lhs - rhs).abs() / scale).max()) < 1e-2
