@@ -211,7 +211,9 @@ SKV_API const char* skv_status_str(skv_status status);
  * on-device wait of the tensor-core kernels launched afterwards by this
  * process (default 2 s).  A wait that runs out sets SKV_ERR_TIMEOUT in the
  * device status word, abandons the work item and lets the kernel finish
- * cleanly.  `limit` <= 0 restores the default.
+ * cleanly.  `limit` == 0 restores the default.  `limit` < 0 is a test mode:
+ * the deadline is -limit ns and every block first waits on a barrier that
+ * nothing ever completes, so the timeout path runs deterministically.
  */
 SKV_API skv_status skv_set_wait_limit(int64_t limit);
 

@@ -125,7 +125,7 @@ skv_status get_ctx(void* stream, Ctx& ctx) {
         }
         ctx.status = g_status_ptr[dev];
         ctx.num_sms = g_num_sms[dev];
-        ctx.wait_limit = g_wait_limit > 0 ? g_wait_limit : 2000000000LL;   // ns
+        ctx.wait_limit = g_wait_limit != 0 ? g_wait_limit : 2000000000LL;   // ns (< 0: test mode)
     }
     ctx.stream = static_cast<cudaStream_t>(stream);
     return SKV_OK;
@@ -299,7 +299,7 @@ uint64_t skv_launch_count(void) { return g_launches.load(std::memory_order_relax
 
 skv_status skv_set_wait_limit(int64_t limit) {
     std::lock_guard<std::mutex> lk(g_mu);
-    g_wait_limit = limit > 0 ? limit : 0;
+    g_wait_limit = limit;
     return SKV_OK;
 }
 

@@ -40,6 +40,7 @@ constexpr long long kTeardownWait = 2000000000LL;    // ns
 
 struct BwdHeader {
     uint64_t kv_full, qd_full[2], qd_empty[2], s_full, ds_full, dq_full, dq_free, mma_fin, meta_full;
+    uint64_t stuck;             // never completed: target of the forced-timeout test mode
     uint32_t tmem_base;
     int abort_flag;
     float lse2[BM];
@@ -120,6 +121,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     const int64_t x0 = int64_t(kt) * BN;
     constexpr int NP = D / 64;
     constexpr uint32_t kTile = BM * D * 2;
+    // test mode (negative limit): the MMA thread first waits on a barrier nothing
+    // completes, so the timeout path runs deterministically
+    const bool stuck_test = wait_limit < 0;
+    if (stuck_test) wait_limit = -wait_limit;
     // the swizzled tiles must start on a 1024-byte boundary inside the allocation
     const bool layout_ok = (tiles_s - base_s) + sizeof(BwdTiles<D>) <= (size_t)kSmemMax;
     int cnt = kv_cnt[kt];
@@ -139,6 +144,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         mbar_init(&hd.dq_free, 128);
         mbar_init(&hd.mma_fin, 1);
         mbar_init(&hd.meta_full, 128);
+        mbar_init(&hd.stuck, 1);
         hd.abort_flag = 0;
         fence_mbar_init();
     }
@@ -165,7 +171,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             int t = 0;
             for (; t < cnt; ++t) {
                 const int st = t & 1;
-                if (t >= 2 && !mbar_wait(&hd.qd_empty[st], ((t - 2) >> 1) & 1, wait_limit)) {
+                if (t >= 2 && !mbar_wait(&hd.qd_empty[st], ((t - 2) >> 1) & 1, wait_limit, &hd.abort_flag)) {
                     atomicExch(&hd.abort_flag, 1);
                     skv::raise_status(status, SKV_ERR_TIMEOUT);
                     break;
@@ -195,12 +201,13 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 atomicExch(&hd.abort_flag, 1);
                 skv::raise_status(status, SKV_ERR_TIMEOUT);
             };
-            bool ok = mbar_wait(&hd.kv_full, 0, wait_limit);
+            bool ok = !(stuck_test && !mbar_wait(&hd.stuck, 0, wait_limit, &hd.abort_flag));
+            if (ok) ok = mbar_wait(&hd.kv_full, 0, wait_limit, &hd.abort_flag);
             if (!ok) fail();
             for (int t = 0; ok && t < cnt; ++t) {
                 const int st = t & 1;
-                if (t > 0 && !mbar_wait(&hd.dq_free, (t - 1) & 1, wait_limit)) { fail(); break; }
-                if (!mbar_wait(&hd.qd_full[st], (t >> 1) & 1, wait_limit)) { fail(); break; }
+                if (t > 0 && !mbar_wait(&hd.dq_free, (t - 1) & 1, wait_limit, &hd.abort_flag)) { fail(); break; }
+                if (!mbar_wait(&hd.qd_full[st], (t >> 1) & 1, wait_limit, &hd.abort_flag)) { fail(); break; }
                 if (*(volatile int*)&hd.abort_flag) break;
                 tc_fence_after();
 #pragma unroll
@@ -217,7 +224,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 }
                 issued = true;
                 mma_commit(&hd.s_full);
-                if (!mbar_wait(&hd.ds_full, t & 1, wait_limit)) { fail(); break; }
+                if (!mbar_wait(&hd.ds_full, t & 1, wait_limit, &hd.abort_flag)) { fail(); break; }
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)      // dV += P^T dO
@@ -247,7 +254,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         const int64_t x = x0 + tid;                 // key row of this thread (S^T, dP^T, dK, dV)
         bool ok = true;
         auto uniform_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-            const bool got = __all_sync(kAll, mbar_wait(bar, parity, wait_limit));
+            const bool got = __all_sync(kAll, mbar_wait(bar, parity, wait_limit, &hd.abort_flag));
             if (!got && lane == 0) {
                 atomicExch(&hd.abort_flag, 1);
                 skv::raise_status(status, SKV_ERR_TIMEOUT);

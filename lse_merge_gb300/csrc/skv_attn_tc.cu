@@ -43,6 +43,7 @@ struct __align__(1024) FwdSmem {
     uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
     uint64_t s_full[2], p_full[2], o_done[2];
     uint64_t mma_fin;
+    uint64_t stuck;             // never completed: target of the forced-timeout test mode
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -94,6 +95,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     constexpr int NP = D / 64;                       // 64-column panels per row
     constexpr uint32_t kTileBytes = BN * D * 2;      // one K or V tile (== Q tile)
 
+    // test mode (negative limit): every block first waits on a barrier nothing
+    // completes, so the timeout path runs deterministically
+    const bool stuck_test = wait_limit < 0;
+    if (stuck_test) wait_limit = -wait_limit;
     TileBounds tb = tile_bounds(s, a, B, Qn, S, qt);
     // once any block of the launch has timed out the result is void: the
     // remaining blocks skip their work instead of each waiting out a deadline
@@ -112,6 +117,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             mbar_init(&sm.o_done[i], 1);
         }
         mbar_init(&sm.mma_fin, 1);
+        mbar_init(&sm.stuck, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -145,7 +151,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 }
                 const int st = n % kStages;
                 if (n >= kStages) {
-                    if (!mbar_wait(&sm.kv_empty[st], ((n - kStages) / kStages) & 1, wait_limit)) {
+                    if (!mbar_wait(&sm.kv_empty[st], ((n - kStages) / kStages) & 1, wait_limit, &sm.abort_flag)) {
                         atomicExch(&sm.abort_flag, 1);
                         skv::raise_status(status, SKV_ERR_TIMEOUT);
                         break;
@@ -186,9 +192,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 skv::raise_status(status, SKV_ERR_TIMEOUT);
                 ok = false;
             };
+            if (stuck_test && !mbar_wait(&sm.stuck, 0, wait_limit, &sm.abort_flag)) fail();
             auto issue_s = [&](int n) {
                 const int st = n % kStages;
-                if (!mbar_wait(&sm.k_full[st], (n / kStages) & 1, wait_limit)) { fail(); return; }
+                if (!mbar_wait(&sm.k_full[st], (n / kStages) & 1, wait_limit, &sm.abort_flag)) { fail(); return; }
                 tc_fence_after();
                 const uint32_t dS = tS + (n & 1) * BN;
 #pragma unroll
@@ -201,8 +208,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 issued = true;
                 mma_commit(&sm.s_full[n & 1]);
             };
-            if (T > 0) {
-                if (!mbar_wait(&sm.q_full, 0, wait_limit)) fail();
+            if (T > 0 && ok) {
+                if (!mbar_wait(&sm.q_full, 0, wait_limit, &sm.abort_flag)) fail();
                 if (ok) issue_s(0);
                 for (int n = 0; n < T && ok; ++n) {
                     if (*(volatile int*)&sm.abort_flag) { ok = false; break; }
@@ -211,8 +218,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                         if (!ok) break;
                     }
                     const int st = n % kStages;
-                    if (!mbar_wait(&sm.p_full[n & 1], (n >> 1) & 1, wait_limit)) { fail(); break; }
-                    if (!mbar_wait(&sm.v_full[st], (n / kStages) & 1, wait_limit)) { fail(); break; }
+                    if (!mbar_wait(&sm.p_full[n & 1], (n >> 1) & 1, wait_limit, &sm.abort_flag)) { fail(); break; }
+                    if (!mbar_wait(&sm.v_full[st], (n / kStages) & 1, wait_limit, &sm.abort_flag)) { fail(); break; }
                     tc_fence_after();
                     const uint32_t aP = tP + (n & 1) * 64;
 #pragma unroll
@@ -247,7 +254,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         int o_waited = 0;
         bool ok = true;
         auto uniform_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-            const bool got = __all_sync(kAll, mbar_wait(bar, parity, wait_limit));
+            const bool got = __all_sync(kAll, mbar_wait(bar, parity, wait_limit, &sm.abort_flag));
             if (!got && lane == 0) {
                 atomicExch(&sm.abort_flag, 1);
                 skv::raise_status(status, SKV_ERR_TIMEOUT);

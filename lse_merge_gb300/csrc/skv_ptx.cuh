@@ -51,14 +51,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Bounded wait for the phase with the given parity to complete: gives up
-// after `limit_ns` nanoseconds of the global timer and returns false (the
-// caller records a timeout and abandons its work).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit_ns) {
+// after `limit_ns` nanoseconds of the global timer, or as soon as the block's
+// abort flag (if given) is set, and returns false (the caller records a
+// timeout and abandons its work).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit_ns,
+                                          const int* abort_flag = nullptr) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
+        if (abort_flag && *reinterpret_cast<const volatile int*>(abort_flag)) return false;
         if (static_cast<long long>(global_timer_ns() - t0) > limit_ns) return false;
     }
 }

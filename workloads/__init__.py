@@ -95,7 +95,11 @@ def qs_sweep(ratio: int, order: str = "lpt") -> Workload:
                     4096, 32, "bf16", 0.5, 0.5, order, True)
 
 
-WORKLOADS = {w.name: w for w in (TINY_FP32, BF16_FWD, PACKED, LONG_1M)}
+# A reduced packed case for ncu captures (inputs > L2, a few GB on the device).
+PROFILE_SMALL = Workload("profile_1x128k", 6, 1, 131072, 512, *_resp(131072), 16, 8, 128, 4096, 8,
+                         "bf16", 0.5, 1.0, "lpt", True)
+
+WORKLOADS = {w.name: w for w in (TINY_FP32, BF16_FWD, PACKED, LONG_1M, PROFILE_SMALL)}
 for _r in (4, 8, 16, 32):
     for _o in ("lpt", "contiguous"):
         _w = qs_sweep(_r, _o)
