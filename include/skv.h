@@ -159,6 +159,32 @@ SKV_API skv_status skv_attn_fwd(const skv_problem* prob, const void* q, const vo
                         void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * skv_attn_fwd without a workspace argument, for callers that may not
+ * allocate device memory (a plug-in whose host framework owns the whole device
+ * memory pool, a latency-critical loop that cannot afford a cudaMalloc that may
+ * synchronise the device, a runtime held to a fixed memory budget).  The paper
+ * has no counterpart to this call; it is a packaging of skv_attn_fwd.
+ *
+ * Same arguments, semantics and outputs as skv_attn_fwd.  The scratch the
+ * forward needs (the per-rank chunk lists) lives in a fixed 128 KiB array in
+ * device memory that every GPU loading the library holds until the process
+ * exits; the call itself allocates nothing.  Problems whose forward workspace
+ * (skv_workspace_bytes(prob, 0)) exceeds 131072 bytes are rejected with
+ * SKV_ERR_WORKSPACE before any launch -- e.g. P <= 1024 ranks with up to
+ * 30 000 chunks fit.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array, and each call rewrites the lists
+ * before reading them (nothing in it has to start at zero), so calls that
+ * overlap on the GPU (on different streams, or from different host threads
+ * without ordering) race and must be serialised by the caller.
+ */
+SKV_API skv_status skv_attn_fwd_static(const skv_problem* prob, const void* q, const void* k, const void* v,
+                                       const int32_t* rank_of_chunk, float* o_part, float* lse_part,
+                                       void* stream);
+
+/*
  * Exact LSE merge of P disjoint partials [Split-KV §4.1, Eq. 4; Alg. 1 line 8]:
  *   lse[r] = log sum_p exp(lse_part[p][r]),
  *   o[r][:] = sum_p exp(lse_part[p][r] - lse[r]) * o_part[p][r][:].

@@ -20,7 +20,7 @@ from . import _lib
 from ._lib import SKV_BF16, SKV_FP32, SkvProblem
 
 __all__ = ["SkvError", "Problem", "chunk_costs", "lpt_order", "contiguous_order", "zigzag_loads",
-           "workspace_bytes", "attn_fwd", "lse_merge", "attn_bwd", "stream_status", "set_wait_limit",
+           "workspace_bytes", "attn_fwd", "attn_fwd_static", "lse_merge", "attn_bwd", "stream_status", "set_wait_limit",
            "forward", "plan"]
 
 
@@ -148,6 +148,20 @@ def attn_fwd(prob: Problem, q, k, v, rank_of_chunk, o_part=None, lse_part=None, 
     ws = _workspace(prob, 0, workspace)
     _check(_lib.load().skv_attn_fwd(prob.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(rank_of_chunk), _ptr(o_part),
                                     _ptr(lse_part), _ptr(ws), ws.numel(), _stream()), "skv_attn_fwd")
+    return o_part, lse_part
+
+
+def attn_fwd_static(prob: Problem, q, k, v, rank_of_chunk, o_part=None, lse_part=None):
+    """attn_fwd without a workspace: the library's fixed device scratch is used
+    instead, for callers that must not allocate device memory.  Calls that
+    overlap on the GPU race on that shared scratch."""
+    dev = q.device
+    if o_part is None:
+        o_part = torch.empty(prob.P, prob.Q, prob.H, prob.d, dtype=torch.float32, device=dev)
+    if lse_part is None:
+        lse_part = torch.empty(prob.P, prob.Q, prob.H, dtype=torch.float32, device=dev)
+    _check(_lib.load().skv_attn_fwd_static(prob.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(rank_of_chunk),
+                                           _ptr(o_part), _ptr(lse_part), _stream()), "skv_attn_fwd_static")
     return o_part, lse_part
 
 
