@@ -87,8 +87,11 @@ size_t bwd_ws_layout(const skv_problem& pb, BwdWs* w, char* base) {
     size_t off = 0;
     const size_t o_ptr = off; off = align256(off + size_t(pb.P + 1) * 4);
     const size_t o_list = off; off = align256(off + size_t(n) * 4);
-    const size_t o_D = off; off = align256(off + size_t(rows) * 4);
-    const size_t o_l2 = off; off = align256(off + size_t(rows) * 4);
+    // D and lse2: row-major [Q][H], or head-major [H][Qp] padded to whole query tiles
+    const int64_t Qp = ((int64_t(pb.n_blocks) * pb.B + 127) / 128) * 128;
+    const int64_t drows = Qp * pb.n_heads;
+    const size_t o_D = off; off = align256(off + size_t(drows) * 4);
+    const size_t o_l2 = off; off = align256(off + size_t(drows) * 4);
     const bool tc = skv_tc::bwd_supported(pb);
     const size_t o_dqp = off; off = align256(off + (tc ? 0 : size_t(pb.P) * rows * pb.head_dim * 4));
     const size_t o_tc = off; off = align256(off + skv_tc::bwd_scratch_bytes(pb));
@@ -253,7 +256,10 @@ skv_status skv_attn_bwd(const skv_problem* pb_in, const void* q, const void* k, 
     BwdWs w;
     bwd_ws_layout(pb, &w, static_cast<char*>(workspace));
     const int n = (int)(pb.S / pb.m);
-    if ((st = skv_internal::launch_bwd_prep(o, dO, lse, pb.dtype, rows, pb.head_dim, w.D, w.lse2, c)) != SKV_OK)
+    const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
+    const int64_t Qp = tc ? ((Qn + 127) / 128) * 128 : Qn;
+    if ((st = skv_internal::launch_bwd_prep(o, dO, lse, pb.dtype, Qn, Qp, pb.n_heads, pb.head_dim, tc, w.D, w.lse2,
+                                            c)) != SKV_OK)
         return st;
     if (tc) {
         // key tiles are visited rank by rank inside the kernel's tile lists; dq^(p)

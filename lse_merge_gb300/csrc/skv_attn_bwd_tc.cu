@@ -33,31 +33,44 @@ namespace {
 using namespace skv_ptx;
 using namespace skv_tcc;
 
-constexpr int kBwdThreads = 192;
+constexpr int kBwdThreads = 320;                     // WG1 warps 0-3, WG2 warps 4-7, MMA 8, TMA 9
 constexpr int kSmemMax = 232448;                     // sm_100-family opt-in maximum per block
-constexpr int kHeaderBytes = 3072;
 constexpr long long kTeardownWait = 2000000000LL;    // ns
 
-struct BwdHeader {
-    uint64_t kv_full, qd_full[2], qd_empty[2], s_full, ds_full, dq_full, dq_free, mma_fin, meta_full;
-    uint64_t stuck;             // never completed: target of the forced-timeout test mode
-    uint32_t tmem_base;
-    int abort_flag;
-    float lse2[BM];
-    float Dr[BM];
-    int32_t rlo[BM];
-    int32_t rhi[BM];
-};
-static_assert(sizeof(BwdHeader) <= kHeaderBytes, "header");
-
 template <int D>
-struct BwdTiles {
+struct BwdTiles {                                    // 1024-byte aligned (128-byte swizzle atoms)
     __nv_bfloat16 k[D / 64][BN * 64];
     __nv_bfloat16 v[D / 64][BN * 64];
     __nv_bfloat16 q[2][D / 64][BM * 64];
     __nv_bfloat16 dO[2][D / 64][BM * 64];
-    __nv_bfloat16 ds[2][BN * 64];       // dS^T [key][q], two 64-query panels
+    __nv_bfloat16 ds[2][BN * 64];                    // dS^T [key][q], two 64-query panels
 };
+
+struct BwdMeta {                                     // per query tile, loaded with its Q/dO stage
+    float lse2[BM];
+    float D[BM];
+};
+
+struct BwdBars {
+    uint64_t kv_full, qd_full[2], qd_empty[2], s_full, dp_full, ds_full, dq_full, dq_free, mma_fin;
+    uint64_t stuck;                                  // never completed: target of the forced-timeout test mode
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+template <int D>
+struct BwdSmem {
+    BwdTiles<D> t;
+    BwdMeta meta[2];
+    BwdBars b;
+};
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
 
 __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
@@ -106,16 +119,22 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                   const float* __restrict__ lse2_g, const float* __restrict__ D_g, const int32_t* __restrict__ s,
-                   const int32_t* __restrict__ a, int B, int64_t Qn, int H, int64_t S, float scale, float scale_log2,
-                   const int4* __restrict__ qtb, const int32_t* __restrict__ kv_cnt,
+                   const float* __restrict__ lse2_hm, const float* __restrict__ D_hm, int64_t Qp,
+                   const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int64_t Qn, int H, int64_t S,
+                   float scale, float scale_log2, const int4* __restrict__ qtb, const int32_t* __restrict__ kv_cnt,
                    const int32_t* __restrict__ kv_list, int n_qt, float* __restrict__ dq, float* __restrict__ dk,
                    float* __restrict__ dv, int* status, long long wait_limit) {
     extern __shared__ unsigned char smem_raw[];
-    BwdHeader& hd = *reinterpret_cast<BwdHeader*>(smem_raw);
     const uint32_t base_s = smem_u32(smem_raw);
-    const uint32_t tiles_s = (base_s + kHeaderBytes + 1023u) & ~1023u;
-    BwdTiles<D>& tl = *reinterpret_cast<BwdTiles<D>*>(smem_raw + (tiles_s - base_s));
+    const uint32_t pad = ((base_s + 1023u) & ~1023u) - base_s;
+    // the swizzled tiles must start on a 1024-byte boundary inside the allocation
+    if (pad + sizeof(BwdSmem<D>) > (size_t)kSmemMax) {
+        if (threadIdx.x == 0) skv::raise_status(status, SKV_ERR_UNSUPPORTED);
+        return;
+    }
+    BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw + pad);
+    BwdTiles<D>& tl = sm.t;
+    BwdBars& bb = sm.b;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kt = blockIdx.x, h = blockIdx.y;
     const int64_t x0 = int64_t(kt) * BN;
@@ -125,106 +144,111 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     // completes, so the timeout path runs deterministically
     const bool stuck_test = wait_limit < 0;
     if (stuck_test) wait_limit = -wait_limit;
-    // the swizzled tiles must start on a 1024-byte boundary inside the allocation
-    const bool layout_ok = (tiles_s - base_s) + sizeof(BwdTiles<D>) <= (size_t)kSmemMax;
     int cnt = kv_cnt[kt];
-    if (!layout_ok || *(volatile int*)status == SKV_ERR_TIMEOUT) cnt = 0;
-    if (!layout_ok && tid == 0) skv::raise_status(status, SKV_ERR_UNSUPPORTED);
+    if (*(volatile int*)status == SKV_ERR_TIMEOUT) cnt = 0;   // launch already void: skip the work
     const int32_t* list = kv_list + int64_t(kt) * n_qt;
 
     if (tid == 0) {
-        mbar_init(&hd.kv_full, 1);
+        mbar_init(&bb.kv_full, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&hd.qd_full[i], 1);
-            mbar_init(&hd.qd_empty[i], 1);
+            mbar_init(&bb.qd_full[i], 1);
+            mbar_init(&bb.qd_empty[i], 1);
         }
-        mbar_init(&hd.s_full, 1);
-        mbar_init(&hd.ds_full, 128);
-        mbar_init(&hd.dq_full, 1);
-        mbar_init(&hd.dq_free, 128);
-        mbar_init(&hd.mma_fin, 1);
-        mbar_init(&hd.meta_full, 128);
-        mbar_init(&hd.stuck, 1);
-        hd.abort_flag = 0;
+        mbar_init(&bb.s_full, 1);
+        mbar_init(&bb.dp_full, 1);
+        mbar_init(&bb.ds_full, 128);
+        mbar_init(&bb.dq_full, 1);
+        mbar_init(&bb.dq_free, 128);
+        mbar_init(&bb.mma_fin, 1);
+        mbar_init(&bb.stuck, 1);
+        bb.abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 4) {
-        tmem_alloc(&hd.tmem_base, 512);
+    if (warp == 8) {
+        tmem_alloc(&bb.tmem_base, 512);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = hd.tmem_base;
+    const uint32_t tmem = bb.tmem_base;
     const uint32_t tA = tmem, tB = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+    auto abort_now = [&]() {
+        atomicExch(&bb.abort_flag, 1);
+        skv::raise_status(status, SKV_ERR_TIMEOUT);
+    };
 
-    if (warp == 5) {
-        // ------------------------------------------------------------ producer
+    if (warp == 9) {
+        // ------------------------------------------------------------ TMA producer
         if (lane == 0 && cnt > 0) {
             prefetch_tensormap(&map_q);
             prefetch_tensormap(&map_do);
-            mbar_arrive_expect_tx(&hd.kv_full, 2 * kTile);
+            mbar_arrive_expect_tx(&bb.kv_full, 2 * kTile);
             for (int c = 0; c < NP; ++c) {
-                tma_load_2d(tl.k[c], &map_k, &hd.kv_full, h * D + c * 64, (int)x0);
-                tma_load_2d(tl.v[c], &map_v, &hd.kv_full, h * D + c * 64, (int)x0);
+                tma_load_2d(tl.k[c], &map_k, &bb.kv_full, h * D + c * 64, (int)x0);
+                tma_load_2d(tl.v[c], &map_v, &bb.kv_full, h * D + c * 64, (int)x0);
             }
             int t = 0;
             for (; t < cnt; ++t) {
                 const int st = t & 1;
-                if (t >= 2 && !mbar_wait(&hd.qd_empty[st], ((t - 2) >> 1) & 1, wait_limit, &hd.abort_flag)) {
-                    atomicExch(&hd.abort_flag, 1);
-                    skv::raise_status(status, SKV_ERR_TIMEOUT);
+                if (t >= 2 && !mbar_wait(&bb.qd_empty[st], ((t - 2) >> 1) & 1, wait_limit, &bb.abort_flag)) {
+                    abort_now();
                     break;
                 }
-                if (*(volatile int*)&hd.abort_flag) break;
+                if (*(volatile int*)&bb.abort_flag) break;
                 const int row = list[t] * BM;
-                mbar_arrive_expect_tx(&hd.qd_full[st], 2 * kTile);
+                mbar_arrive_expect_tx(&bb.qd_full[st], 2 * kTile + 2 * BM * 4);
                 for (int c = 0; c < NP; ++c) {
-                    tma_load_2d(tl.q[st][c], &map_q, &hd.qd_full[st], h * D + c * 64, row);
-                    tma_load_2d(tl.dO[st][c], &map_do, &hd.qd_full[st], h * D + c * 64, row);
+                    tma_load_2d(tl.q[st][c], &map_q, &bb.qd_full[st], h * D + c * 64, row);
+                    tma_load_2d(tl.dO[st][c], &map_do, &bb.qd_full[st], h * D + c * 64, row);
                 }
+                bulk_load(sm.meta[st].lse2, lse2_hm + int64_t(h) * Qp + row, BM * 4, &bb.qd_full[st]);
+                bulk_load(sm.meta[st].D, D_hm + int64_t(h) * Qp + row, BM * 4, &bb.qd_full[st]);
             }
-            mbar_wait(&hd.kv_full, 0, kTeardownWait);
+            // every copy issued has landed before the block exits
+            mbar_wait(&bb.kv_full, 0, kTeardownWait);
             for (int st = 0; st < 2 && st < t; ++st) {
                 const int last = st + ((t - 1 - st) >> 1) * 2;
-                mbar_wait(&hd.qd_full[st], (last >> 1) & 1, kTeardownWait);
+                mbar_wait(&bb.qd_full[st], (last >> 1) & 1, kTeardownWait);
             }
         }
-    } else if (warp == 4) {
+    } else if (warp == 8) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && cnt > 0) {
             constexpr uint32_t idS = idesc_bf16_f32(BN, BM, 0, 0);    // M = keys, N = queries, K = d
             constexpr uint32_t idKV = idesc_bf16_f32(BN, D, 0, 1);    // M = keys, N = d, K = queries
             constexpr uint32_t idQ = idesc_bf16_f32(BM, D, 1, 1);     // M = queries, N = d, K = keys
             bool issued = false;
-            auto fail = [&]() {
-                atomicExch(&hd.abort_flag, 1);
-                skv::raise_status(status, SKV_ERR_TIMEOUT);
-            };
-            bool ok = !(stuck_test && !mbar_wait(&hd.stuck, 0, wait_limit, &hd.abort_flag));
-            if (ok) ok = mbar_wait(&hd.kv_full, 0, wait_limit, &hd.abort_flag);
-            if (!ok) fail();
-            for (int t = 0; ok && t < cnt; ++t) {
-                const int st = t & 1;
-                if (t > 0 && !mbar_wait(&hd.dq_free, (t - 1) & 1, wait_limit, &hd.abort_flag)) { fail(); break; }
-                if (!mbar_wait(&hd.qd_full[st], (t >> 1) & 1, wait_limit, &hd.abort_flag)) { fail(); break; }
-                if (*(volatile int*)&hd.abort_flag) break;
-                tc_fence_after();
+            bool ok = !(stuck_test && !mbar_wait(&bb.stuck, 0, wait_limit, &bb.abort_flag));
+            if (ok) ok = mbar_wait(&bb.kv_full, 0, wait_limit, &bb.abort_flag);
+            auto issue_s = [&](int st) {                   // S^T = K Q^T -> A
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk & 3) * 32;
                     mma_ss(tA, smem_desc(smem_u32(tl.k[kk >> 2]) + off, 16, 1024),
                            smem_desc(smem_u32(tl.q[st][kk >> 2]) + off, 16, 1024), idS, kk > 0);
                 }
+                mma_commit(&bb.s_full);
+            };
+            auto issue_dp = [&](int st) {                  // dP^T = V dO^T -> B
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk & 3) * 32;
                     mma_ss(tB, smem_desc(smem_u32(tl.v[kk >> 2]) + off, 16, 1024),
                            smem_desc(smem_u32(tl.dO[st][kk >> 2]) + off, 16, 1024), idS, kk > 0);
                 }
+                mma_commit(&bb.dp_full);
+            };
+            if (ok) ok = mbar_wait(&bb.qd_full[0], 0, wait_limit, &bb.abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                issue_dp(0);
                 issued = true;
-                mma_commit(&hd.s_full);
-                if (!mbar_wait(&hd.ds_full, t & 1, wait_limit, &hd.abort_flag)) { fail(); break; }
+            }
+            for (int t = 0; ok && t < cnt; ++t) {
+                const int st = t & 1;
+                if (!mbar_wait(&bb.ds_full, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)      // dV += P^T dO
@@ -236,163 +260,187 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                            smem_desc(smem_u32(tl.q[st][0]) + kk * 2048, BM * 128, 1024), idKV,
                            (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)      // dQ = dS K
+                for (int kk = 0; kk < BN / 16; ++kk)      // dQ = dS K -> B
                     mma_ss(tB, smem_desc(smem_u32(tl.ds[0]) + kk * 2048, BN * 128, 1024),
                            smem_desc(smem_u32(tl.k[0]) + kk * 2048, BN * 128, 1024), idQ, kk > 0);
-                mma_commit(&hd.dq_full);
-                mma_commit(&hd.qd_empty[st]);
+                mma_commit(&bb.dq_full);
+                mma_commit(&bb.qd_empty[st]);
+                if (t + 1 < cnt) {
+                    const int st1 = (t + 1) & 1;
+                    if (!mbar_wait(&bb.qd_full[st1], ((t + 1) >> 1) & 1, wait_limit, &bb.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // S_{t+1} overwrites A, whose bf16 P_t the dV MMA above reads: MMAs of one
+                    // thread execute in issue order
+                    issue_s(st1);
+                    if (!mbar_wait(&bb.dq_free, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_dp(st1);
+                }
             }
+            if (!ok) abort_now();
             if (issued) {
-                mma_commit(&hd.mma_fin);
-                if (!mbar_wait(&hd.mma_fin, 0, kTeardownWait)) skv::raise_status(status, SKV_ERR_TIMEOUT);
+                mma_commit(&bb.mma_fin);
+                if (!mbar_wait(&bb.mma_fin, 0, kTeardownWait)) skv::raise_status(status, SKV_ERR_TIMEOUT);
             }
+        } else if (lane == 0 && stuck_test) {
+            // (no work) nothing to time out on
         }
     } else {
-        // ------------------------------------------------------------ compute
         constexpr unsigned kAll = 0xffffffffu;
-        const uint32_t lane_base = uint32_t(warp * 32) << 16;
-        const int64_t x = x0 + tid;                 // key row of this thread (S^T, dP^T, dK, dV)
+        const int wg_warp = warp & 3;                    // TMEM lane quadrant
+        const uint32_t lane_base = uint32_t(wg_warp * 32) << 16;
+        const int r = wg_warp * 32 + lane;               // TMEM lane of this thread
         bool ok = true;
         auto uniform_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-            const bool got = __all_sync(kAll, mbar_wait(bar, parity, wait_limit, &hd.abort_flag));
-            if (!got && lane == 0) {
-                atomicExch(&hd.abort_flag, 1);
-                skv::raise_status(status, SKV_ERR_TIMEOUT);
-            }
+            const bool got = __all_sync(kAll, mbar_wait(bar, parity, wait_limit, &bb.abort_flag));
+            if (!got && lane == 0) abort_now();
             return got;
         };
-        unsigned char* ds_bytes = reinterpret_cast<unsigned char*>(&tl.ds[0][0]);
-        for (int t = 0; t < cnt; ++t) {
-            const int qt = list[t];
-            const int64_t row0 = int64_t(qt) * BM;
-            // the 128 compute threads share the tile's row data through shared
-            // memory; they sync on mbarriers (bounded waits), never bar.sync:
-            // previous tile's rows are read by everyone once ds_full(t-1) completed
-            if (t > 0 && !uniform_wait(&hd.ds_full, (t - 1) & 1)) { ok = false; break; }
-            {
-                const int64_t r = row0 + tid;
-                if (r < Qn) {
-                    hd.lse2[tid] = lse2_g[r * H + h];
-                    hd.Dr[tid] = D_g[r * H + h];
-                    int64_t lo, hi;
-                    skv::block_window(s, a, (int)(r / B), S, lo, hi);
-                    hd.rlo[tid] = (int32_t)lo;
-                    hd.rhi[tid] = (int32_t)hi;
-                } else {
-                    hd.lse2[tid] = INFINITY;         // rows past the end contribute nothing
-                    hd.Dr[tid] = 0.f;
-                    hd.rlo[tid] = 0;
-                    hd.rhi[tid] = 0;
-                }
-            }
-            mbar_arrive(&hd.meta_full);
-            if (!uniform_wait(&hd.meta_full, t & 1)) { ok = false; break; }
-            const int4 b = qtb[qt];
-            const bool full = (x0 >= b.z) && (x0 + BN <= b.w);
-            if (__any_sync(kAll, *(volatile int*)&hd.abort_flag != 0)) { ok = false; break; }
-            if (!uniform_wait(&hd.s_full, t & 1)) { ok = false; break; }
-            tc_fence_after();
-            // 32 query columns at a time: P^T (fp32 in registers, bf16 to TMEM A),
-            // then dS^T from the matching dP^T columns (bf16 to shared memory)
+        if (warp < 4) {
+            // -------------------------------------------------------- WG1: P^T and dS^T
+            const int64_t x = x0 + r;                    // key row (S^T, dP^T, dK)
+            unsigned char* ds_bytes = reinterpret_cast<unsigned char*>(&tl.ds[0][0]);
+            for (int t = 0; t < cnt; ++t) {
+                const int st = t & 1;
+                const int qt = list[t];
+                const int64_t row0 = int64_t(qt) * BM;
+                const int4 bnd = qtb[qt];
+                const bool full = (x0 >= bnd.z) && (x0 + BN <= bnd.w);
+                if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
+                if (!uniform_wait(&bb.qd_full[st], (t >> 1) & 1)) { ok = false; break; }
+                const BwdMeta& md = sm.meta[st];
+                if (!uniform_wait(&bb.s_full, t & 1)) { ok = false; break; }
+                tc_fence_after();
+                float pr[BM];
+#pragma unroll
+                for (int c = 0; c < BM / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(tA + lane_base + c * 32, rr);
+                    tmem_ld_wait();
+                    uint32_t keep = 0xffffffffu;          // columns whose query row sees key x
+                    if (!full) {                          // boundary tile: each query row's own window
+                        keep = 0u;
 #pragma unroll 1
-            for (int c = 0; c < BM / 32; ++c) {
-                uint32_t rr[32];
-                tmem_ld32(tA + lane_base + c * 32, rr);
-                tmem_ld_wait();
-                float pr[32];
+                        for (int j = 0; j < 32; ++j) {
+                            const int64_t qr = row0 + c * 32 + j;
+                            int64_t lo = 0, hi = 0;
+                            if (qr < Qn) skv::block_window(s, a, (int)(qr / B), S, lo, hi);
+                            if (lo <= x && x < hi) keep |= 1u << j;
+                        }
+                    }
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int col = c * 32 + j;
-                    float pv = ex2(fmaf(__uint_as_float(rr[j]), scale_log2, -hd.lse2[col]));
-                    if (!full && !(hd.rlo[col] <= x && x < hd.rhi[col])) pv = 0.f;
-                    pr[j] = pv;
+                    for (int j = 0; j < 32; ++j)
+                        pr[c * 32 + j] = ((keep >> j) & 1u)
+                                             ? ex2(fmaf(__uint_as_float(rr[j]), scale_log2, -md.lse2[c * 32 + j]))
+                                             : 0.f;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(pr[c * 32 + 2 * j], pr[c * 32 + 2 * j + 1]);
+                    // bf16 P^T columns [32c, 32c+32) -> TMEM columns [16c, 16c+16) of A: those S^T
+                    // columns were read already
+                    tmem_st16(tA + lane_base + c * 16, pk);
                 }
-                uint32_t pk[16];
+                if (!uniform_wait(&bb.dp_full, t & 1)) { ok = false; break; }
+                tc_fence_after();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(pr[2 * j], pr[2 * j + 1]);
-                // P^T columns [32c, 32c+32) -> bf16 pairs in TMEM columns [16c, 16c+16); S^T
-                // columns < 32(c+1) have been read already, so the store cannot clobber unread S
-                tmem_st16(tA + lane_base + c * 16, pk);
-                tmem_ld32(tB + lane_base + c * 32, rr);
-                tmem_ld_wait();
+                for (int c = 0; c < BM / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(tB + lane_base + c * 32, rr);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c0 = c * 32 + 2 * j;
-                    const float d0 = pr[2 * j] * (__uint_as_float(rr[2 * j]) - hd.Dr[c0]);
-                    const float d1 = pr[2 * j + 1] * (__uint_as_float(rr[2 * j + 1]) - hd.Dr[c0 + 1]);
-                    pk[j] = pack_bf16(d0, d1);
+                    for (int j = 0; j < 16; ++j) {
+                        const int c0 = c * 32 + 2 * j;
+                        pk[j] = pack_bf16(pr[c0] * (__uint_as_float(rr[2 * j]) - md.D[c0]),
+                                          pr[c0 + 1] * (__uint_as_float(rr[2 * j + 1]) - md.D[c0 + 1]));
+                    }
+                    // query columns [32c, 32c+32) = panel c/2, 16-byte chunks (c%2)*4 .. +3
+                    unsigned char* rowp = ds_bytes + (c >> 1) * (BN * 128) + r * 128;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int chunk = (c & 1) * 4 + u;
+                        *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) << 4)) =
+                            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                    }
                 }
-                // columns [32c, 32c+32) = panel c/2, 16-byte chunks (c%2)*4 .. +3
-                unsigned char* rowp = ds_bytes + (c >> 1) * (BN * 128) + tid * 128;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int chunk = (c & 1) * 4 + u;
-                    *reinterpret_cast<uint4*>(rowp + ((chunk ^ (tid & 7)) << 4)) =
-                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                }
+                tmem_st_wait();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bb.ds_full);
             }
-            tmem_st_wait();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&hd.ds_full);
-            if (!uniform_wait(&hd.dq_full, t & 1)) { ok = false; break; }
-            tc_fence_after();
-            {
-                const int64_t qrow = row0 + tid;         // TMEM lane = query row for dQ
-                float* dst = dq + (qrow * H + h) * D;
+            // dK rows of this key tile (scaled), once every MMA has completed
+            const bool aborted = __any_sync(kAll, *(volatile int*)&bb.abort_flag != 0);
+            float* dkr = dk + (x * H + h) * D;
+            if (cnt > 0 && ok && !aborted && uniform_wait(&bb.dq_full, (cnt - 1) & 1)) {
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t rk[32];
+                    tmem_ld32(tdK + lane_base + c * 32, rk);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        __stcs(reinterpret_cast<float4*>(dkr + c * 32 + j),
+                               make_float4(scale * __uint_as_float(rk[j]), scale * __uint_as_float(rk[j + 1]),
+                                           scale * __uint_as_float(rk[j + 2]), scale * __uint_as_float(rk[j + 3])));
+                }
+            } else if (cnt == 0) {
+#pragma unroll
+                for (int j = 0; j < D; j += 4) __stcs(reinterpret_cast<float4*>(dkr + j), make_float4(0.f, 0.f, 0.f, 0.f));
+            }
+        } else {
+            // -------------------------------------------------------- WG2: dQ -> dq (fp32 reductions)
+            for (int t = 0; t < cnt; ++t) {
+                const int64_t qrow = int64_t(list[t]) * BM + r;   // TMEM lane = query row for dQ
+                if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
+                if (!uniform_wait(&bb.dq_full, t & 1)) { ok = false; break; }
+                tc_fence_after();
+                float qv[D];
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t rr[32];
                     tmem_ld32(tB + lane_base + c * 32, rr);
                     tmem_ld_wait();
-                    if (qrow < Qn) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            red_add4(dst + c * 32 + j, scale * __uint_as_float(rr[j]),
-                                     scale * __uint_as_float(rr[j + 1]), scale * __uint_as_float(rr[j + 2]),
-                                     scale * __uint_as_float(rr[j + 3]));
-                    }
+                    for (int j = 0; j < 32; ++j) qv[c * 32 + j] = scale * __uint_as_float(rr[j]);
+                }
+                tc_fence_before();
+                mbar_arrive(&bb.dq_free);                 // B may now take dP of the next tile
+                if (qrow < Qn) {
+                    float* dst = dq + (qrow * H + h) * D;
+#pragma unroll
+                    for (int j = 0; j < D; j += 4) red_add4(dst + j, qv[j], qv[j + 1], qv[j + 2], qv[j + 3]);
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&hd.dq_free);
-        }
-        // dK, dV rows of this key tile (zeros when no query sees it)
-        const bool aborted = __any_sync(kAll, *(volatile int*)&hd.abort_flag != 0);
-        if (!aborted && layout_ok) {
-            float* dkr = dk + (x * H + h) * D;
+            // dV rows of this key tile
+            const int64_t x = x0 + r;
             float* dvr = dv + (x * H + h) * D;
-            if (cnt > 0 && ok) {
+            const bool aborted = __any_sync(kAll, *(volatile int*)&bb.abort_flag != 0);
+            if (cnt > 0 && ok && !aborted) {
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
-                    uint32_t rk[32], rv[32];
-                    tmem_ld32(tdK + lane_base + c * 32, rk);
+                    uint32_t rv[32];
                     tmem_ld32(tdV + lane_base + c * 32, rv);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        __stcs(reinterpret_cast<float4*>(dkr + c * 32 + j),
-                               make_float4(scale * __uint_as_float(rk[j]), scale * __uint_as_float(rk[j + 1]),
-                                           scale * __uint_as_float(rk[j + 2]), scale * __uint_as_float(rk[j + 3])));
+                    for (int j = 0; j < 32; j += 4)
                         __stcs(reinterpret_cast<float4*>(dvr + c * 32 + j),
                                make_float4(__uint_as_float(rv[j]), __uint_as_float(rv[j + 1]),
                                            __uint_as_float(rv[j + 2]), __uint_as_float(rv[j + 3])));
-                    }
                 }
             } else if (cnt == 0) {
-                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int j = 0; j < D; j += 4) {
-                    __stcs(reinterpret_cast<float4*>(dkr + j), z);
-                    __stcs(reinterpret_cast<float4*>(dvr + j), z);
-                }
+                for (int j = 0; j < D; j += 4) __stcs(reinterpret_cast<float4*>(dvr + j), make_float4(0.f, 0.f, 0.f, 0.f));
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -423,10 +471,11 @@ size_t scratch_layout(const skv_problem& pb, BwdScratch* w, char* base) {
 
 template <int D>
 skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const void* v, const void* dO,
-                      const float* lse2, const float* Dv, float* dq, float* dk, float* dv, void* scratch,
+                      const float* lse2_hm, const float* D_hm, float* dq, float* dk, float* dv, void* scratch,
                       const skv_host::Ctx& c) {
     const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
     const int n_qt = (int)((Qn + BM - 1) / BM);
+    const int64_t Qp = int64_t(n_qt) * BM;
     const int n_kv = (int)(pb.S / BN);
     BwdScratch w;
     scratch_layout(pb, &w, static_cast<char*>(scratch));
@@ -443,9 +492,9 @@ skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const
     auto kern = attn_bwd_tc_kernel<D>;
     SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax));
     const dim3 grid((unsigned)n_kv, (unsigned)pb.n_heads);
-    kern<<<grid, kBwdThreads, kSmemMax, c.stream>>>(mq, mdo, mk, mv, lse2, Dv, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S,
-                                                    pb.scale, pb.scale * 1.4426950408889634f, w.qtb, w.cnt, w.list,
-                                                    n_qt, dq, dk, dv, c.status, c.wait_limit);
+    kern<<<grid, kBwdThreads, kSmemMax, c.stream>>>(mq, mdo, mk, mv, lse2_hm, D_hm, Qp, pb.s, pb.a, pb.B, Qn,
+                                                    pb.n_heads, pb.S, pb.scale, pb.scale * 1.4426950408889634f, w.qtb,
+                                                    w.cnt, w.list, n_qt, dq, dk, dv, c.status, c.wait_limit);
     SKV_LAUNCHED();
     return SKV_OK;
 }

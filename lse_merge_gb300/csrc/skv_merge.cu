@@ -149,22 +149,38 @@ skv_status merge_dispatch(const float* o_part, const float* lse_part, int P, int
 }
 
 // D_r = sum_t dO[r,t] * o[r,t] and lse2_r = lse_r * log2(e): one warp per row.
+// Input rows are (query q, head h) = q*H + h.  Output index: q*H + h
+// (row-major, Qp == Qn), or h*Qp + q (head-major, Qp = Qn rounded up to the
+// query tile) with pad rows q >= Qn set to lse2 = +inf, D = 0 so that they
+// contribute nothing downstream.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ dO, const float* __restrict__ lse,
-                int64_t rows, int d, float* __restrict__ D, float* __restrict__ lse2) {
+                int64_t Qn, int64_t Qp, int H, int d, bool head_major, float* __restrict__ D,
+                float* __restrict__ lse2) {
     const int lane = threadIdx.x & 31;
     const int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t r = w; r < rows; r += nw) {
+    const int64_t vrows = Qp * H;
+    for (int64_t vr = w; vr < vrows; vr += nw) {
+        const int64_t q = vr / H, h = vr - (vr / H) * H;
+        const int64_t out = head_major ? h * Qp + q : vr;
+        if (q >= Qn) {
+            if (lane == 0) {
+                D[out] = 0.f;
+                lse2[out] = INFINITY;
+            }
+            continue;
+        }
+        const int64_t r = q * H + h;
         float acc = 0.f;
         for (int t = lane; t < d; t += 32)
             acc = fmaf(skv::to_f32(o[r * d + t]), skv::to_f32(dO[r * d + t]), acc);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (lane == 0) {
-            D[r] = acc;
-            lse2[r] = lse[r] * 1.4426950408889634f;
+            D[out] = acc;
+            lse2[out] = lse[r] * 1.4426950408889634f;
         }
     }
 }
@@ -193,17 +209,19 @@ skv_status launch_merge(const float* o_part, const float* lse_part, int P, int64
     return merge_dispatch(o_part, lse_part, P, rows, d, static_cast<float*>(o), lse, c);
 }
 
-skv_status launch_bwd_prep(const void* o, const void* dO, const float* lse, skv_dtype dt, int64_t rows, int d,
-                           float* D, float* lse2, const skv_host::Ctx& c) {
-    if (rows == 0) return SKV_OK;
-    int64_t blocks = (rows + (kThreads / 32) - 1) / (kThreads / 32);
+skv_status launch_bwd_prep(const void* o, const void* dO, const float* lse, skv_dtype dt, int64_t Qn, int64_t Qp,
+                           int H, int d, bool head_major, float* D, float* lse2, const skv_host::Ctx& c) {
+    const int64_t vrows = Qp * H;
+    if (vrows == 0) return SKV_OK;
+    int64_t blocks = (vrows + (kThreads / 32) - 1) / (kThreads / 32);
     if (blocks > int64_t(c.num_sms) * 8) blocks = int64_t(c.num_sms) * 8;
     if (dt == SKV_BF16)
         bwd_prep_kernel<<<(unsigned)blocks, kThreads, 0, c.stream>>>(
-            static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, rows, d, D, lse2);
+            static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, Qn, Qp, H, d,
+            head_major, D, lse2);
     else
         bwd_prep_kernel<<<(unsigned)blocks, kThreads, 0, c.stream>>>(
-            static_cast<const float*>(o), static_cast<const float*>(dO), lse, rows, d, D, lse2);
+            static_cast<const float*>(o), static_cast<const float*>(dO), lse, Qn, Qp, H, d, head_major, D, lse2);
     SKV_LAUNCHED();
     return SKV_OK;
 }
