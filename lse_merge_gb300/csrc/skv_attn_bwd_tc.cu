@@ -33,7 +33,8 @@ namespace {
 using namespace skv_ptx;
 using namespace skv_tcc;
 
-constexpr int kBwdThreads = 320;                     // WG1 warps 0-3, WG2 warps 4-7, MMA 8, TMA 9
+constexpr int kBwdThreads = 448;                     // WG1 warps 0-7, WG2 warps 8-11, MMA 12, TMA 13
+constexpr int kMmaWarp = 12, kTmaWarp = 13;
 constexpr int kSmemMax = 232448;                     // sm_100-family opt-in maximum per block
 constexpr long long kTeardownWait = 2000000000LL;    // ns
 
@@ -156,7 +157,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         }
         mbar_init(&bb.s_full, 1);
         mbar_init(&bb.dp_full, 1);
-        mbar_init(&bb.ds_full, 128);
+        mbar_init(&bb.ds_full, 256);
         mbar_init(&bb.dq_full, 1);
         mbar_init(&bb.dq_free, 128);
         mbar_init(&bb.mma_fin, 1);
@@ -164,7 +165,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         bb.abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&bb.tmem_base, 512);
         tmem_relinquish();
     }
@@ -178,7 +179,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         skv::raise_status(status, SKV_ERR_TIMEOUT);
     };
 
-    if (warp == 9) {
+    if (warp == kTmaWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && cnt > 0) {
             prefetch_tensormap(&map_q);
@@ -212,7 +213,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 mbar_wait(&bb.qd_full[st], (last >> 1) & 1, kTeardownWait);
             }
         }
-    } else if (warp == 8) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && cnt > 0) {
             constexpr uint32_t idS = idesc_bf16_f32(BN, BM, 0, 0);    // M = keys, N = queries, K = d
@@ -250,34 +251,39 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 const int st = t & 1;
                 if (!mbar_wait(&bb.ds_full, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
                 tc_fence_after();
+                // dV += P^T dO.  bf16 P^T of query columns [64h, 64h+64) sits in TMEM
+                // columns [64h, 64h+32) of A (each half-warpgroup writes inside its own half)
 #pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)      // dV += P^T dO
-                    mma_ts(tdV, tA + kk * 8, smem_desc(smem_u32(tl.dO[st][0]) + kk * 2048, BM * 128, 1024), idKV,
+                for (int kk = 0; kk < BM / 16; ++kk)
+                    mma_ts(tdV, tA + (kk >> 2) * 64 + (kk & 3) * 8,
+                           smem_desc(smem_u32(tl.dO[st][0]) + kk * 2048, BM * 128, 1024), idKV,
                            (t > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)      // dK += dS^T Q
-                    mma_ss(tdK, smem_desc(smem_u32(tl.ds[kk >> 2]) + (kk & 3) * 32, 16, 1024),
-                           smem_desc(smem_u32(tl.q[st][0]) + kk * 2048, BM * 128, 1024), idKV,
-                           (t > 0 || kk > 0) ? 1u : 0u);
+                // S_{t+1} overwrites A right behind the dV MMA that reads P_t from it:
+                // the MMAs of one thread execute in issue order
+                const bool more = t + 1 < cnt;
+                if (more) {
+                    if (!mbar_wait(&bb.qd_full[(t + 1) & 1], ((t + 1) >> 1) & 1, wait_limit, &bb.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_s((t + 1) & 1);
+                }
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)      // dQ = dS K -> B
                     mma_ss(tB, smem_desc(smem_u32(tl.ds[0]) + kk * 2048, BN * 128, 1024),
                            smem_desc(smem_u32(tl.k[0]) + kk * 2048, BN * 128, 1024), idQ, kk > 0);
                 mma_commit(&bb.dq_full);
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk)      // dK += dS^T Q
+                    mma_ss(tdK, smem_desc(smem_u32(tl.ds[kk >> 2]) + (kk & 3) * 32, 16, 1024),
+                           smem_desc(smem_u32(tl.q[st][0]) + kk * 2048, BM * 128, 1024), idKV,
+                           (t > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bb.qd_empty[st]);
-                if (t + 1 < cnt) {
-                    const int st1 = (t + 1) & 1;
-                    if (!mbar_wait(&bb.qd_full[st1], ((t + 1) >> 1) & 1, wait_limit, &bb.abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // S_{t+1} overwrites A, whose bf16 P_t the dV MMA above reads: MMAs of one
-                    // thread execute in issue order
-                    issue_s(st1);
+                if (more) {
                     if (!mbar_wait(&bb.dq_free, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    issue_dp(st1);
+                    issue_dp((t + 1) & 1);
                 }
             }
             if (!ok) abort_now();
@@ -285,8 +291,6 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 mma_commit(&bb.mma_fin);
                 if (!mbar_wait(&bb.mma_fin, 0, kTeardownWait)) skv::raise_status(status, SKV_ERR_TIMEOUT);
             }
-        } else if (lane == 0 && stuck_test) {
-            // (no work) nothing to time out on
         }
     } else {
         constexpr unsigned kAll = 0xffffffffu;
@@ -299,10 +303,13 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             if (!got && lane == 0) abort_now();
             return got;
         };
-        if (warp < 4) {
+        if (warp < 8) {
             // -------------------------------------------------------- WG1: P^T and dS^T
+            // warp w owns TMEM lanes (keys) of quadrant w%4 and query columns
+            // [64*hf, 64*hf+64) with hf = w/4
+            const int hf = warp >> 2;
             const int64_t x = x0 + r;                    // key row (S^T, dP^T, dK)
-            unsigned char* ds_bytes = reinterpret_cast<unsigned char*>(&tl.ds[0][0]);
+            unsigned char* ds_panel = reinterpret_cast<unsigned char*>(&tl.ds[hf][0]) + r * 128;
             for (int t = 0; t < cnt; ++t) {
                 const int st = t & 1;
                 const int qt = list[t];
@@ -314,18 +321,19 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 const BwdMeta& md = sm.meta[st];
                 if (!uniform_wait(&bb.s_full, t & 1)) { ok = false; break; }
                 tc_fence_after();
-                float pr[BM];
+                float pr[64];
 #pragma unroll
-                for (int c = 0; c < BM / 32; ++c) {
+                for (int c = 0; c < 2; ++c) {
+                    const int col0 = hf * 64 + c * 32;
                     uint32_t rr[32];
-                    tmem_ld32(tA + lane_base + c * 32, rr);
+                    tmem_ld32(tA + lane_base + col0, rr);
                     tmem_ld_wait();
                     uint32_t keep = 0xffffffffu;          // columns whose query row sees key x
                     if (!full) {                          // boundary tile: each query row's own window
                         keep = 0u;
 #pragma unroll 1
                         for (int j = 0; j < 32; ++j) {
-                            const int64_t qr = row0 + c * 32 + j;
+                            const int64_t qr = row0 + col0 + j;
                             int64_t lo = 0, hi = 0;
                             if (qr < Qn) skv::block_window(s, a, (int)(qr / B), S, lo, hi);
                             if (lo <= x && x < hi) keep |= 1u << j;
@@ -334,35 +342,35 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         pr[c * 32 + j] = ((keep >> j) & 1u)
-                                             ? ex2(fmaf(__uint_as_float(rr[j]), scale_log2, -md.lse2[c * 32 + j]))
+                                             ? ex2(fmaf(__uint_as_float(rr[j]), scale_log2, -md.lse2[col0 + j]))
                                              : 0.f;
                     uint32_t pk[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(pr[c * 32 + 2 * j], pr[c * 32 + 2 * j + 1]);
-                    // bf16 P^T columns [32c, 32c+32) -> TMEM columns [16c, 16c+16) of A: those S^T
-                    // columns were read already
-                    tmem_st16(tA + lane_base + c * 16, pk);
+                    // bf16 pairs of these 32 columns -> TMEM columns [64hf + 16c, +16): inside
+                    // this warp's own half, over S^T columns it has read already
+                    tmem_st16(tA + lane_base + hf * 64 + c * 16, pk);
                 }
                 if (!uniform_wait(&bb.dp_full, t & 1)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < BM / 32; ++c) {
+                for (int c = 0; c < 2; ++c) {
+                    const int col0 = hf * 64 + c * 32;
                     uint32_t rr[32];
-                    tmem_ld32(tB + lane_base + c * 32, rr);
+                    tmem_ld32(tB + lane_base + col0, rr);
                     tmem_ld_wait();
                     uint32_t pk[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const int c0 = c * 32 + 2 * j;
-                        pk[j] = pack_bf16(pr[c0] * (__uint_as_float(rr[2 * j]) - md.D[c0]),
-                                          pr[c0 + 1] * (__uint_as_float(rr[2 * j + 1]) - md.D[c0 + 1]));
+                        const int cc = c * 32 + 2 * j;
+                        pk[j] = pack_bf16(pr[cc] * (__uint_as_float(rr[2 * j]) - md.D[col0 + 2 * j]),
+                                          pr[cc + 1] * (__uint_as_float(rr[2 * j + 1]) - md.D[col0 + 2 * j + 1]));
                     }
-                    // query columns [32c, 32c+32) = panel c/2, 16-byte chunks (c%2)*4 .. +3
-                    unsigned char* rowp = ds_bytes + (c >> 1) * (BN * 128) + r * 128;
+                    // query columns [64hf + 32c, +32) = panel hf, 16-byte chunks 4c .. 4c+3
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int chunk = (c & 1) * 4 + u;
-                        *reinterpret_cast<uint4*>(rowp + ((chunk ^ (r & 7)) << 4)) =
+                        const int chunk = c * 4 + u;
+                        *reinterpret_cast<uint4*>(ds_panel + ((chunk ^ (r & 7)) << 4)) =
                             make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
                     }
                 }
@@ -371,25 +379,29 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 tc_fence_before();
                 mbar_arrive(&bb.ds_full);
             }
-            // dK rows of this key tile (scaled), once every MMA has completed
+            // dK rows of this key tile (scaled; columns split between the two halves)
+            // once every MMA of the block has completed
             const bool aborted = __any_sync(kAll, *(volatile int*)&bb.abort_flag != 0);
             float* dkr = dk + (x * H + h) * D;
-            if (cnt > 0 && ok && !aborted && uniform_wait(&bb.dq_full, (cnt - 1) & 1)) {
+            constexpr int kHalf = D / 2;
+            if (cnt > 0 && ok && !aborted && uniform_wait(&bb.mma_fin, 0)) {
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < kHalf / 32; ++c) {
+                    const int col0 = hf * kHalf + c * 32;
                     uint32_t rk[32];
-                    tmem_ld32(tdK + lane_base + c * 32, rk);
+                    tmem_ld32(tdK + lane_base + col0, rk);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
-                        __stcs(reinterpret_cast<float4*>(dkr + c * 32 + j),
+                        __stcs(reinterpret_cast<float4*>(dkr + col0 + j),
                                make_float4(scale * __uint_as_float(rk[j]), scale * __uint_as_float(rk[j + 1]),
                                            scale * __uint_as_float(rk[j + 2]), scale * __uint_as_float(rk[j + 3])));
                 }
             } else if (cnt == 0) {
 #pragma unroll
-                for (int j = 0; j < D; j += 4) __stcs(reinterpret_cast<float4*>(dkr + j), make_float4(0.f, 0.f, 0.f, 0.f));
+                for (int j = 0; j < kHalf; j += 4)
+                    __stcs(reinterpret_cast<float4*>(dkr + hf * kHalf + j), make_float4(0.f, 0.f, 0.f, 0.f));
             }
         } else {
             // -------------------------------------------------------- WG2: dQ -> dq (fp32 reductions)
@@ -398,28 +410,29 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
                 if (!uniform_wait(&bb.dq_full, t & 1)) { ok = false; break; }
                 tc_fence_after();
-                float qv[D];
+                float* dst = dq + (qrow * H + h) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t rr[32];
                     tmem_ld32(tB + lane_base + c * 32, rr);
                     tmem_ld_wait();
+                    if (c == D / 32 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(&bb.dq_free);         // B may now take dP of the next tile
+                    }
+                    if (qrow < Qn) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) qv[c * 32 + j] = scale * __uint_as_float(rr[j]);
-                }
-                tc_fence_before();
-                mbar_arrive(&bb.dq_free);                 // B may now take dP of the next tile
-                if (qrow < Qn) {
-                    float* dst = dq + (qrow * H + h) * D;
-#pragma unroll
-                    for (int j = 0; j < D; j += 4) red_add4(dst + j, qv[j], qv[j + 1], qv[j + 2], qv[j + 3]);
+                        for (int j = 0; j < 32; j += 4)
+                            red_add4(dst + c * 32 + j, scale * __uint_as_float(rr[j]), scale * __uint_as_float(rr[j + 1]),
+                                     scale * __uint_as_float(rr[j + 2]), scale * __uint_as_float(rr[j + 3]));
+                    }
                 }
             }
             // dV rows of this key tile
             const int64_t x = x0 + r;
             float* dvr = dv + (x * H + h) * D;
             const bool aborted = __any_sync(kAll, *(volatile int*)&bb.abort_flag != 0);
-            if (cnt > 0 && ok && !aborted) {
+            if (cnt > 0 && ok && !aborted && uniform_wait(&bb.mma_fin, 0)) {
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -440,7 +453,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
