@@ -50,6 +50,9 @@ struct BwdTiles {                                    // 1024-byte aligned (128-b
 struct BwdMeta {                                     // per query tile, loaded with its Q/dO stage
     float lse2[BM];
     float D[BM];
+    int4 bnd;                                        // the tile's key bounds (written by the producer)
+    int qt;                                          // the query tile index
+    int pad_[3];
 };
 
 struct BwdBars {
@@ -197,7 +200,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     break;
                 }
                 if (*(volatile int*)&bb.abort_flag) break;
-                const int row = list[t] * BM;
+                const int qt = list[t];
+                const int row = qt * BM;
+                sm.meta[st].qt = qt;                     // made visible by the arrive below
+                sm.meta[st].bnd = qtb[qt];
                 mbar_arrive_expect_tx(&bb.qd_full[st], 2 * kTile + 2 * BM * 4);
                 for (int c = 0; c < NP; ++c) {
                     tma_load_2d(tl.q[st][c], &map_q, &bb.qd_full[st], h * D + c * 64, row);
@@ -299,7 +305,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         const int r = wg_warp * 32 + lane;               // TMEM lane of this thread
         bool ok = true;
         auto uniform_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-            const bool got = __all_sync(kAll, mbar_wait(bar, parity, wait_limit, &bb.abort_flag));
+            const bool got = mbar_wait_warp(bar, parity, wait_limit, &bb.abort_flag);
             if (!got && lane == 0) abort_now();
             return got;
         };
@@ -312,22 +318,24 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             unsigned char* ds_panel = reinterpret_cast<unsigned char*>(&tl.ds[hf][0]) + r * 128;
             for (int t = 0; t < cnt; ++t) {
                 const int st = t & 1;
-                const int qt = list[t];
-                const int64_t row0 = int64_t(qt) * BM;
-                const int4 bnd = qtb[qt];
-                const bool full = (x0 >= bnd.z) && (x0 + BN <= bnd.w);
                 if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
                 if (!uniform_wait(&bb.qd_full[st], (t >> 1) & 1)) { ok = false; break; }
                 const BwdMeta& md = sm.meta[st];
+                const int64_t row0 = int64_t(md.qt) * BM;
+                const int4 bnd = md.bnd;
+                const bool full = (x0 >= bnd.z) && (x0 + BN <= bnd.w);
                 if (!uniform_wait(&bb.s_full, t & 1)) { ok = false; break; }
                 tc_fence_after();
-                float pr[64];
+                // both 32-column chunks of S^T are loaded before one wait; P^T is kept as
+                // the bf16 pairs the dV MMA consumes and dS^T is formed from those values
+                uint32_t sraw[2][32];
+                tmem_ld32(tA + lane_base + hf * 64, sraw[0]);
+                tmem_ld32(tA + lane_base + hf * 64 + 32, sraw[1]);
+                tmem_ld_wait();
+                uint32_t pk[2][16];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int col0 = hf * 64 + c * 32;
-                    uint32_t rr[32];
-                    tmem_ld32(tA + lane_base + col0, rr);
-                    tmem_ld_wait();
                     uint32_t keep = 0xffffffffu;          // columns whose query row sees key x
                     if (!full) {                          // boundary tile: each query row's own window
                         keep = 0u;
@@ -339,39 +347,52 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                             if (lo <= x && x < hi) keep |= 1u << j;
                         }
                     }
+                    const float4* l4 = reinterpret_cast<const float4*>(md.lse2 + col0);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        pr[c * 32 + j] = ((keep >> j) & 1u)
-                                             ? ex2(fmaf(__uint_as_float(rr[j]), scale_log2, -md.lse2[col0 + j]))
-                                             : 0.f;
-                    uint32_t pk[16];
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 l = l4[j4];
+                        const float lv[4] = {l.x, l.y, l.z, l.w};
+                        float pv[4];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) pk[j] = pack_bf16(pr[c * 32 + 2 * j], pr[c * 32 + 2 * j + 1]);
+                        for (int u = 0; u < 4; ++u) {
+                            const int j = 4 * j4 + u;
+                            pv[u] = ((keep >> j) & 1u) ? ex2(fmaf(__uint_as_float(sraw[c][j]), scale_log2, -lv[u]))
+                                                       : 0.f;
+                        }
+                        pk[c][2 * j4] = pack_bf16(pv[0], pv[1]);
+                        pk[c][2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
+                    }
                     // bf16 pairs of these 32 columns -> TMEM columns [64hf + 16c, +16): inside
                     // this warp's own half, over S^T columns it has read already
-                    tmem_st16(tA + lane_base + hf * 64 + c * 16, pk);
+                    tmem_st16(tA + lane_base + hf * 64 + c * 16, pk[c]);
                 }
                 if (!uniform_wait(&bb.dp_full, t & 1)) { ok = false; break; }
                 tc_fence_after();
+                uint32_t draw[2][32];
+                tmem_ld32(tB + lane_base + hf * 64, draw[0]);
+                tmem_ld32(tB + lane_base + hf * 64 + 32, draw[1]);
+                tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int col0 = hf * 64 + c * 32;
-                    uint32_t rr[32];
-                    tmem_ld32(tB + lane_base + col0, rr);
-                    tmem_ld_wait();
-                    uint32_t pk[16];
+                    uint32_t dk2[16];
+                    const float4* d4 = reinterpret_cast<const float4*>(md.D + col0);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int cc = c * 32 + 2 * j;
-                        pk[j] = pack_bf16(pr[cc] * (__uint_as_float(rr[2 * j]) - md.D[col0 + 2 * j]),
-                                          pr[cc + 1] * (__uint_as_float(rr[2 * j + 1]) - md.D[col0 + 2 * j + 1]));
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 dd = d4[j4];
+                        const float2 p01 = unpack_bf16(pk[c][2 * j4]);
+                        const float2 p23 = unpack_bf16(pk[c][2 * j4 + 1]);
+                        dk2[2 * j4] = pack_bf16(p01.x * (__uint_as_float(draw[c][4 * j4]) - dd.x),
+                                                p01.y * (__uint_as_float(draw[c][4 * j4 + 1]) - dd.y));
+                        dk2[2 * j4 + 1] = pack_bf16(p23.x * (__uint_as_float(draw[c][4 * j4 + 2]) - dd.z),
+                                                    p23.y * (__uint_as_float(draw[c][4 * j4 + 3]) - dd.w));
                     }
                     // query columns [64hf + 32c, +32) = panel hf, 16-byte chunks 4c .. 4c+3
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int chunk = c * 4 + u;
                         *reinterpret_cast<uint4*>(ds_panel + ((chunk ^ (r & 7)) << 4)) =
-                            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                            make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
                     }
                 }
                 tmem_st_wait();
@@ -405,26 +426,32 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             }
         } else {
             // -------------------------------------------------------- WG2: dQ -> dq (fp32 reductions)
+            int qt_next = cnt > 0 ? list[0] : 0;
             for (int t = 0; t < cnt; ++t) {
-                const int64_t qrow = int64_t(list[t]) * BM + r;   // TMEM lane = query row for dQ
+                const int64_t qrow = int64_t(qt_next) * BM + r;   // TMEM lane = query row for dQ
+                if (t + 1 < cnt) qt_next = list[t + 1];        // prefetched for the next tile
                 if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
                 if (!uniform_wait(&bb.dq_full, t & 1)) { ok = false; break; }
                 tc_fence_after();
                 float* dst = dq + (qrow * H + h) * D;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(tB + lane_base + c * 32, rr);
+                for (int c = 0; c < D / 32; c += 2) {         // two TMEM loads per wait
+                    uint32_t rr[2][32];
+                    tmem_ld32(tB + lane_base + c * 32, rr[0]);
+                    tmem_ld32(tB + lane_base + c * 32 + 32, rr[1]);
                     tmem_ld_wait();
-                    if (c == D / 32 - 1) {
+                    if (c + 2 >= D / 32) {
                         tc_fence_before();
                         mbar_arrive(&bb.dq_free);         // B may now take dP of the next tile
                     }
                     if (qrow < Qn) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            red_add4(dst + c * 32 + j, scale * __uint_as_float(rr[j]), scale * __uint_as_float(rr[j + 1]),
-                                     scale * __uint_as_float(rr[j + 2]), scale * __uint_as_float(rr[j + 3]));
+                        for (int u = 0; u < 2; ++u)
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4)
+                                red_add4(dst + (c + u) * 32 + j, scale * __uint_as_float(rr[u][j]),
+                                         scale * __uint_as_float(rr[u][j + 1]), scale * __uint_as_float(rr[u][j + 2]),
+                                         scale * __uint_as_float(rr[u][j + 3]));
                     }
                 }
             }

@@ -254,7 +254,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         int o_waited = 0;
         bool ok = true;
         auto uniform_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-            const bool got = __all_sync(kAll, mbar_wait(bar, parity, wait_limit, &sm.abort_flag));
+            const bool got = mbar_wait_warp(bar, parity, wait_limit, &sm.abort_flag);
             if (!got && lane == 0) {
                 atomicExch(&sm.abort_flag, 1);
                 skv::raise_status(status, SKV_ERR_TIMEOUT);
@@ -277,13 +277,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             if (!uniform_wait(&sm.s_full[n & 1], (n >> 1) & 1)) { ok = false; break; }
             tc_fence_after();
             float sc[BN];
+            {
+                uint32_t raw[BN / 32][32];               // all chunks in flight before one wait
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t rr[32];
-                tmem_ld32(tS + (n & 1) * BN + lane_base + c * 32, rr);
+                for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + (n & 1) * BN + lane_base + c * 32, raw[c]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) sc[c * 32 + j] = __uint_as_float(rr[j]);
+                for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sc[c * 32 + j] = __uint_as_float(raw[c][j]);
             }
             const bool full = (x0 >= tb.flo) && (x0 + BN <= tb.fhi);
             if (!full) {

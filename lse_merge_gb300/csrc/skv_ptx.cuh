@@ -66,6 +66,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
     }
 }
 
+// The same wait made by every lane of a converged warp, with one verdict for
+// all lanes (all lanes polling measured faster than one lane plus a shuffle).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, long long limit_ns,
+                                               const int* abort_flag = nullptr) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns, abort_flag));
+}
+
 // --------------------------------------------------------------------- TMA
 
 // 2D tiled bulk tensor load global -> shared, completion counted in bytes on
@@ -216,6 +223,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+__device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
 __device__ __forceinline__ float ex2(float x) {
