@@ -261,14 +261,10 @@ skv_status skv_attn_bwd(const skv_problem* pb_in, const void* q, const void* k, 
     if ((st = skv_internal::launch_bwd_prep(o, dO, lse, pb.dtype, Qn, Qp, pb.n_heads, pb.head_dim, tc, w.D, w.lse2,
                                             c)) != SKV_OK)
         return st;
-    if (tc) {
-        // key tiles are visited rank by rank inside the kernel's tile lists; dq^(p)
-        // of every rank is summed into dq by fp32 reductions
-        skv::RankCSR none{nullptr, nullptr};
-        return skv_tc::launch_attn_bwd_tc(pb, q, k, v, dO, w.lse2, w.D, none, dq, dk, dv, w.tc, c);
-    }
     if ((st = skv_internal::launch_rank_csr(rank_of_chunk, n, pb.P, w.csr_ptr, w.csr_list, c)) != SKV_OK) return st;
     skv::RankCSR csr{w.csr_ptr, w.csr_list};
+    if (tc)   // dk_p, dv_p per key tile; dq = sum_p dq^(p) accumulated rank by rank per query tile
+        return skv_tc::launch_attn_bwd_tc(pb, q, k, v, dO, w.lse2, w.D, csr, dq, dk, dv, w.tc, c);
     if ((st = skv_internal::launch_attn_bwd_simt(pb, q, k, v, dO, lse, w.D, csr, w.dq_part, dk, dv, c)) != SKV_OK)
         return st;
     return skv_internal::launch_dq_sum(w.dq_part, pb.P, rows, pb.head_dim, dq, c);

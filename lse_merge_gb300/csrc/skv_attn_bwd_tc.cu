@@ -3,24 +3,25 @@
 // "Split-KV: Efficient Context Parallelism for Training Diffusion Drafters",
 // Alg. 1 lines 15-17 in merged form: with the global log-sum-exp l_r and
 // D_r = dO_r . o_r, every rank's score gradient is dS = P (dP - D) with
-// P = exp(z - l).  Each virtual rank p owns the key tiles of its chunks, so
-// its dk_p / dv_p rows are written by exactly one thread block each, and its
-// dq^(p) contributions are summed into dq by fp32 reduction adds (the
-// reduce-scatter of Alg. 1 line 17 made local).
+// P = exp(z - l).  Two kernels:
 //
-// Key-stationary: one thread block owns a 128-key tile and one head and walks
-// the 128-row query tiles whose windows meet the tile (the tile-skip list
-// built by skv_kv_list_kernel; masked-out query tiles are never loaded).  Per
-// query tile t (TMEM lane = key for S^T, dP^T, dV, dK; = query row for dQ):
-//   S^T  = K Q_t^T          (SS)  -> TMEM A [0,128)
-//   dP^T = V dO_t^T         (SS)  -> TMEM B [128,256)
-//   compute warps: P^T = exp2(S^T scale log2e - l2), bf16 P^T -> TMEM A[0,64);
-//                  dS^T = P^T (dP^T - D), bf16 -> shared memory (swizzled)
-//   dV  += P^T dO_t         (TS)  -> TMEM [256, 256+D)
-//   dK  += dS^T Q_t         (SS)  -> TMEM [384, 384+D)
-//   dQ_t = dS K             (SS, dS^T read MN-major) -> TMEM B
-//   compute warps: dq[rows] += scale dQ_t (red.global.add.v4.f32)
-// Roles (192 threads): warps 0-3 compute, warp 4 MMA issuer, warp 5 TMA.
+//  * attn_bwd_dkdv_tc_kernel -- key-stationary.  One thread block owns a
+//    128-key tile and a head (the tile belongs to exactly one rank, so dk_p and
+//    dv_p rows are written once, no atomics) and walks the query tiles of its
+//    tile-skip list (built by qtile_bounds_kernel / kv_list_kernel; masked-out
+//    query tiles are never loaded).  Per query tile t:
+//      S^T = K Q_t^T, dP^T = V dO_t^T (SS) -> TMEM A, B
+//      eight warps: P^T = exp2(S^T scale log2e - l2) (bf16 -> TMEM A),
+//                   dS^T = P^T (dP^T - D) (bf16 -> swizzled shared memory)
+//      dV += P^T dO_t (TS), dK += dS^T Q_t (SS)
+//  * attn_bwd_dq_tc_kernel -- query-stationary.  One thread block owns a
+//    128-row query tile and a head and walks, rank by rank, the key tiles of
+//    every rank's chunks that meet the tile's windows: dq = sum_p dq^(p)
+//    (Alg. 1 line 17) is accumulated in TMEM and written once.  Per key tile:
+//      S = Q K^T, dP = dO V^T (SS); eight warps form dS (bf16 -> TMEM over S);
+//      dQ += dS K (TS).
+// Recomputing S and dP in the second kernel costs two extra GEMMs per tile pair
+// but removes every dq reduction from the key-stationary loop.
 #include <cuda.h>
 #include <math.h>
 
@@ -33,41 +34,8 @@ namespace {
 using namespace skv_ptx;
 using namespace skv_tcc;
 
-constexpr int kBwdThreads = 448;                     // WG1 warps 0-7, WG2 warps 8-11, MMA 12, TMA 13
-constexpr int kMmaWarp = 12, kTmaWarp = 13;
 constexpr int kSmemMax = 232448;                     // sm_100-family opt-in maximum per block
 constexpr long long kTeardownWait = 2000000000LL;    // ns
-
-template <int D>
-struct BwdTiles {                                    // 1024-byte aligned (128-byte swizzle atoms)
-    __nv_bfloat16 k[D / 64][BN * 64];
-    __nv_bfloat16 v[D / 64][BN * 64];
-    __nv_bfloat16 q[2][D / 64][BM * 64];
-    __nv_bfloat16 dO[2][D / 64][BM * 64];
-    __nv_bfloat16 ds[2][BN * 64];                    // dS^T [key][q], two 64-query panels
-};
-
-struct BwdMeta {                                     // per query tile, loaded with its Q/dO stage
-    float lse2[BM];
-    float D[BM];
-    int4 bnd;                                        // the tile's key bounds (written by the producer)
-    int qt;                                          // the query tile index
-    int pad_[3];
-};
-
-struct BwdBars {
-    uint64_t kv_full, qd_full[2], qd_empty[2], s_full, dp_full, ds_full, dq_full, dq_free, mma_fin;
-    uint64_t stuck;                                  // never completed: target of the forced-timeout test mode
-    uint32_t tmem_base;
-    int abort_flag;
-};
-
-template <int D>
-struct BwdSmem {
-    BwdTiles<D> t;
-    BwdMeta meta[2];
-    BwdBars b;
-};
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -75,12 +43,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
-
-__device__ __forceinline__ void red_add4(float* p, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-
 
 // ---------------------------------------------------------------- tile lists
 
@@ -117,28 +79,62 @@ __global__ void kv_list_kernel(const int4* __restrict__ qtb, int n_qt, int n_kv,
     if (lane == 0) cnt[warp] = n;
 }
 
-// ------------------------------------------------------------------ kernel
+// =============================================================== dK / dV
+
+constexpr int kKvThreads = 320;                      // compute warps 0-7, MMA 8, TMA 9
+constexpr int kKvMma = 8, kKvTma = 9;
 
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
-                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                   const float* __restrict__ lse2_hm, const float* __restrict__ D_hm, int64_t Qp,
-                   const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int64_t Qn, int H, int64_t S,
-                   float scale, float scale_log2, const int4* __restrict__ qtb, const int32_t* __restrict__ kv_cnt,
-                   const int32_t* __restrict__ kv_list, int n_qt, float* __restrict__ dq, float* __restrict__ dk,
-                   float* __restrict__ dv, int* status, long long wait_limit) {
+struct KvTiles {                                     // 1024-byte aligned (128-byte swizzle atoms)
+    __nv_bfloat16 k[D / 64][BN * 64];
+    __nv_bfloat16 v[D / 64][BN * 64];
+    __nv_bfloat16 q[2][D / 64][BM * 64];
+    __nv_bfloat16 dO[2][D / 64][BM * 64];
+    __nv_bfloat16 ds[2][BN * 64];                    // dS^T [key][q], two 64-query panels
+};
+
+struct KvMeta {                                      // per query tile, loaded with its Q/dO stage
+    float lse2[BM];
+    float D[BM];
+    int4 bnd;                                        // the tile's key bounds (written by the producer)
+    int qt;                                          // the query tile index
+    int pad_[3];
+};
+
+struct KvBars {
+    uint64_t kv_full, qd_full[2], qd_empty[2], s_full, dp_full, ds_full, mma_fin;
+    uint64_t stuck;                                  // never completed: target of the forced-timeout test mode
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+template <int D>
+struct KvSmem {
+    KvTiles<D> t;
+    KvMeta meta[2];
+    KvBars b;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kKvThreads, 1)
+attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+                        const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                        const float* __restrict__ lse2_hm, const float* __restrict__ D_hm, int64_t Qp,
+                        const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int64_t Qn, int H,
+                        int64_t S, float scale, float scale_log2, const int4* __restrict__ qtb,
+                        const int32_t* __restrict__ kv_cnt, const int32_t* __restrict__ kv_list, int n_qt,
+                        float* __restrict__ dk, float* __restrict__ dv, int* status, long long wait_limit) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t base_s = smem_u32(smem_raw);
     const uint32_t pad = ((base_s + 1023u) & ~1023u) - base_s;
     // the swizzled tiles must start on a 1024-byte boundary inside the allocation
-    if (pad + sizeof(BwdSmem<D>) > (size_t)kSmemMax) {
+    if (pad + sizeof(KvSmem<D>) > (size_t)kSmemMax) {
         if (threadIdx.x == 0) skv::raise_status(status, SKV_ERR_UNSUPPORTED);
         return;
     }
-    BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw + pad);
-    BwdTiles<D>& tl = sm.t;
-    BwdBars& bb = sm.b;
+    KvSmem<D>& sm = *reinterpret_cast<KvSmem<D>*>(smem_raw + pad);
+    KvTiles<D>& tl = sm.t;
+    KvBars& bb = sm.b;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kt = blockIdx.x, h = blockIdx.y;
     const int64_t x0 = int64_t(kt) * BN;
@@ -161,14 +157,12 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         mbar_init(&bb.s_full, 1);
         mbar_init(&bb.dp_full, 1);
         mbar_init(&bb.ds_full, 256);
-        mbar_init(&bb.dq_full, 1);
-        mbar_init(&bb.dq_free, 128);
         mbar_init(&bb.mma_fin, 1);
         mbar_init(&bb.stuck, 1);
         bb.abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kKvMma) {
         tmem_alloc(&bb.tmem_base, 512);
         tmem_relinquish();
     }
@@ -182,7 +176,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         skv::raise_status(status, SKV_ERR_TIMEOUT);
     };
 
-    if (warp == kTmaWarp) {
+    if (warp == kKvTma) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && cnt > 0) {
             prefetch_tensormap(&map_q);
@@ -219,12 +213,11 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 mbar_wait(&bb.qd_full[st], (last >> 1) & 1, kTeardownWait);
             }
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kKvMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && cnt > 0) {
             constexpr uint32_t idS = idesc_bf16_f32(BN, BM, 0, 0);    // M = keys, N = queries, K = d
             constexpr uint32_t idKV = idesc_bf16_f32(BN, D, 0, 1);    // M = keys, N = d, K = queries
-            constexpr uint32_t idQ = idesc_bf16_f32(BM, D, 1, 1);     // M = queries, N = d, K = keys
             bool issued = false;
             bool ok = !(stuck_test && !mbar_wait(&bb.stuck, 0, wait_limit, &bb.abort_flag));
             if (ok) ok = mbar_wait(&bb.kv_full, 0, wait_limit, &bb.abort_flag);
@@ -258,7 +251,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 if (!mbar_wait(&bb.ds_full, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 // dV += P^T dO.  bf16 P^T of query columns [64h, 64h+64) sits in TMEM
-                // columns [64h, 64h+32) of A (each half-warpgroup writes inside its own half)
+                // columns [64h, 64h+32) of A (each half of the compute warps writes inside its half)
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
                     mma_ts(tdV, tA + (kk >> 2) * 64 + (kk & 3) * 8,
@@ -276,21 +269,13 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     issue_s((t + 1) & 1);
                 }
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)      // dQ = dS K -> B
-                    mma_ss(tB, smem_desc(smem_u32(tl.ds[0]) + kk * 2048, BN * 128, 1024),
-                           smem_desc(smem_u32(tl.k[0]) + kk * 2048, BN * 128, 1024), idQ, kk > 0);
-                mma_commit(&bb.dq_full);
-#pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)      // dK += dS^T Q
                     mma_ss(tdK, smem_desc(smem_u32(tl.ds[kk >> 2]) + (kk & 3) * 32, 16, 1024),
                            smem_desc(smem_u32(tl.q[st][0]) + kk * 2048, BM * 128, 1024), idKV,
                            (t > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bb.qd_empty[st]);
-                if (more) {
-                    if (!mbar_wait(&bb.dq_free, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_dp((t + 1) & 1);
-                }
+                // B held dP_t, which the compute warps finished reading before ds_full
+                if (more) issue_dp((t + 1) & 1);
             }
             if (!ok) abort_now();
             if (issued) {
@@ -299,192 +284,467 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             }
         }
     } else {
+        // ------------------------------------------------------------ compute warps 0-7
+        // warp w owns TMEM lanes (keys) of quadrant w%4 and query columns
+        // [64*hf, 64*hf+64) with hf = w/4
         constexpr unsigned kAll = 0xffffffffu;
-        const int wg_warp = warp & 3;                    // TMEM lane quadrant
-        const uint32_t lane_base = uint32_t(wg_warp * 32) << 16;
-        const int r = wg_warp * 32 + lane;               // TMEM lane of this thread
+        const int quad = warp & 3, hf = warp >> 2;
+        const uint32_t lane_base = uint32_t(quad * 32) << 16;
+        const int r = quad * 32 + lane;                  // TMEM lane = key row
+        const int64_t x = x0 + r;
         bool ok = true;
         auto uniform_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
             const bool got = mbar_wait_warp(bar, parity, wait_limit, &bb.abort_flag);
             if (!got && lane == 0) abort_now();
             return got;
         };
-        if (warp < 8) {
-            // -------------------------------------------------------- WG1: P^T and dS^T
-            // warp w owns TMEM lanes (keys) of quadrant w%4 and query columns
-            // [64*hf, 64*hf+64) with hf = w/4
-            const int hf = warp >> 2;
-            const int64_t x = x0 + r;                    // key row (S^T, dP^T, dK)
-            unsigned char* ds_panel = reinterpret_cast<unsigned char*>(&tl.ds[hf][0]) + r * 128;
-            for (int t = 0; t < cnt; ++t) {
-                const int st = t & 1;
-                if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
-                if (!uniform_wait(&bb.qd_full[st], (t >> 1) & 1)) { ok = false; break; }
-                const BwdMeta& md = sm.meta[st];
-                const int64_t row0 = int64_t(md.qt) * BM;
-                const int4 bnd = md.bnd;
-                const bool full = (x0 >= bnd.z) && (x0 + BN <= bnd.w);
-                if (!uniform_wait(&bb.s_full, t & 1)) { ok = false; break; }
-                tc_fence_after();
-                // both 32-column chunks of S^T are loaded before one wait; P^T is kept as
-                // the bf16 pairs the dV MMA consumes and dS^T is formed from those values
-                uint32_t sraw[2][32];
-                tmem_ld32(tA + lane_base + hf * 64, sraw[0]);
-                tmem_ld32(tA + lane_base + hf * 64 + 32, sraw[1]);
-                tmem_ld_wait();
-                uint32_t pk[2][16];
+        unsigned char* ds_panel = reinterpret_cast<unsigned char*>(&tl.ds[hf][0]) + r * 128;
+        for (int t = 0; t < cnt; ++t) {
+            const int st = t & 1;
+            if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
+            if (!uniform_wait(&bb.qd_full[st], (t >> 1) & 1)) { ok = false; break; }
+            const KvMeta& md = sm.meta[st];
+            const int64_t row0 = int64_t(md.qt) * BM;
+            const int4 bnd = md.bnd;
+            const bool full = (x0 >= bnd.z) && (x0 + BN <= bnd.w);
+            if (!uniform_wait(&bb.s_full, t & 1)) { ok = false; break; }
+            tc_fence_after();
+            // both 32-column chunks of S^T are loaded before one wait; P^T is kept as
+            // the bf16 pairs the dV MMA consumes and dS^T is formed from those values
+            uint32_t sraw[2][32];
+            tmem_ld32(tA + lane_base + hf * 64, sraw[0]);
+            tmem_ld32(tA + lane_base + hf * 64 + 32, sraw[1]);
+            tmem_ld_wait();
+            uint32_t pk[2][16];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int col0 = hf * 64 + c * 32;
-                    uint32_t keep = 0xffffffffu;          // columns whose query row sees key x
-                    if (!full) {                          // boundary tile: each query row's own window
-                        keep = 0u;
+            for (int c = 0; c < 2; ++c) {
+                const int col0 = hf * 64 + c * 32;
+                uint32_t keep = 0xffffffffu;              // columns whose query row sees key x
+                if (!full) {                              // boundary tile: each query row's own window
+                    keep = 0u;
 #pragma unroll 1
-                        for (int j = 0; j < 32; ++j) {
-                            const int64_t qr = row0 + col0 + j;
-                            int64_t lo = 0, hi = 0;
-                            if (qr < Qn) skv::block_window(s, a, (int)(qr / B), S, lo, hi);
-                            if (lo <= x && x < hi) keep |= 1u << j;
-                        }
+                    for (int j = 0; j < 32; ++j) {
+                        const int64_t qr = row0 + col0 + j;
+                        int64_t lo = 0, hi = 0;
+                        if (qr < Qn) skv::block_window(s, a, (int)(qr / B), S, lo, hi);
+                        if (lo <= x && x < hi) keep |= 1u << j;
                     }
-                    const float4* l4 = reinterpret_cast<const float4*>(md.lse2 + col0);
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 l = l4[j4];
-                        const float lv[4] = {l.x, l.y, l.z, l.w};
-                        float pv[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int j = 4 * j4 + u;
-                            pv[u] = ((keep >> j) & 1u) ? ex2(fmaf(__uint_as_float(sraw[c][j]), scale_log2, -lv[u]))
-                                                       : 0.f;
-                        }
-                        pk[c][2 * j4] = pack_bf16(pv[0], pv[1]);
-                        pk[c][2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
-                    }
-                    // bf16 pairs of these 32 columns -> TMEM columns [64hf + 16c, +16): inside
-                    // this warp's own half, over S^T columns it has read already
-                    tmem_st16(tA + lane_base + hf * 64 + c * 16, pk[c]);
                 }
-                if (!uniform_wait(&bb.dp_full, t & 1)) { ok = false; break; }
-                tc_fence_after();
-                uint32_t draw[2][32];
-                tmem_ld32(tB + lane_base + hf * 64, draw[0]);
-                tmem_ld32(tB + lane_base + hf * 64 + 32, draw[1]);
-                tmem_ld_wait();
+                const float4* l4 = reinterpret_cast<const float4*>(md.lse2 + col0);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int col0 = hf * 64 + c * 32;
-                    uint32_t dk2[16];
-                    const float4* d4 = reinterpret_cast<const float4*>(md.D + col0);
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 dd = d4[j4];
-                        const float2 p01 = unpack_bf16(pk[c][2 * j4]);
-                        const float2 p23 = unpack_bf16(pk[c][2 * j4 + 1]);
-                        dk2[2 * j4] = pack_bf16(p01.x * (__uint_as_float(draw[c][4 * j4]) - dd.x),
-                                                p01.y * (__uint_as_float(draw[c][4 * j4 + 1]) - dd.y));
-                        dk2[2 * j4 + 1] = pack_bf16(p23.x * (__uint_as_float(draw[c][4 * j4 + 2]) - dd.z),
-                                                    p23.y * (__uint_as_float(draw[c][4 * j4 + 3]) - dd.w));
-                    }
-                    // query columns [64hf + 32c, +32) = panel hf, 16-byte chunks 4c .. 4c+3
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 l = l4[j4];
+                    const float lv[4] = {l.x, l.y, l.z, l.w};
+                    float pv[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int chunk = c * 4 + u;
-                        *reinterpret_cast<uint4*>(ds_panel + ((chunk ^ (r & 7)) << 4)) =
-                            make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
+                        const int j = 4 * j4 + u;
+                        pv[u] = ((keep >> j) & 1u) ? ex2(fmaf(__uint_as_float(sraw[c][j]), scale_log2, -lv[u]))
+                                                   : 0.f;
                     }
+                    pk[c][2 * j4] = pack_bf16(pv[0], pv[1]);
+                    pk[c][2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
                 }
-                tmem_st_wait();
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(&bb.ds_full);
+                // bf16 pairs of these 32 columns -> TMEM columns [64hf + 16c, +16): inside
+                // this warp's own half, over S^T columns it has read already
+                tmem_st16(tA + lane_base + hf * 64 + c * 16, pk[c]);
             }
-            // dK rows of this key tile (scaled; columns split between the two halves)
-            // once every MMA of the block has completed
-            const bool aborted = __any_sync(kAll, *(volatile int*)&bb.abort_flag != 0);
-            float* dkr = dk + (x * H + h) * D;
-            constexpr int kHalf = D / 2;
-            if (cnt > 0 && ok && !aborted && uniform_wait(&bb.mma_fin, 0)) {
-                tc_fence_after();
+            if (!uniform_wait(&bb.dp_full, t & 1)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t draw[2][32];
+            tmem_ld32(tB + lane_base + hf * 64, draw[0]);
+            tmem_ld32(tB + lane_base + hf * 64 + 32, draw[1]);
+            tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < kHalf / 32; ++c) {
-                    const int col0 = hf * kHalf + c * 32;
-                    uint32_t rk[32];
-                    tmem_ld32(tdK + lane_base + col0, rk);
-                    tmem_ld_wait();
+            for (int c = 0; c < 2; ++c) {
+                const int col0 = hf * 64 + c * 32;
+                uint32_t d2[16];
+                const float4* d4 = reinterpret_cast<const float4*>(md.D + col0);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        __stcs(reinterpret_cast<float4*>(dkr + col0 + j),
-                               make_float4(scale * __uint_as_float(rk[j]), scale * __uint_as_float(rk[j + 1]),
-                                           scale * __uint_as_float(rk[j + 2]), scale * __uint_as_float(rk[j + 3])));
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 dd = d4[j4];
+                    const float2 p01 = unpack_bf16(pk[c][2 * j4]);
+                    const float2 p23 = unpack_bf16(pk[c][2 * j4 + 1]);
+                    d2[2 * j4] = pack_bf16(p01.x * (__uint_as_float(draw[c][4 * j4]) - dd.x),
+                                           p01.y * (__uint_as_float(draw[c][4 * j4 + 1]) - dd.y));
+                    d2[2 * j4 + 1] = pack_bf16(p23.x * (__uint_as_float(draw[c][4 * j4 + 2]) - dd.z),
+                                               p23.y * (__uint_as_float(draw[c][4 * j4 + 3]) - dd.w));
                 }
-            } else if (cnt == 0) {
+                // query columns [64hf + 32c, +32) = panel hf, 16-byte chunks 4c .. 4c+3
 #pragma unroll
-                for (int j = 0; j < kHalf; j += 4)
-                    __stcs(reinterpret_cast<float4*>(dkr + hf * kHalf + j), make_float4(0.f, 0.f, 0.f, 0.f));
-            }
-        } else {
-            // -------------------------------------------------------- WG2: dQ -> dq (fp32 reductions)
-            int qt_next = cnt > 0 ? list[0] : 0;
-            for (int t = 0; t < cnt; ++t) {
-                const int64_t qrow = int64_t(qt_next) * BM + r;   // TMEM lane = query row for dQ
-                if (t + 1 < cnt) qt_next = list[t + 1];        // prefetched for the next tile
-                if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
-                if (!uniform_wait(&bb.dq_full, t & 1)) { ok = false; break; }
-                tc_fence_after();
-                float* dst = dq + (qrow * H + h) * D;
-#pragma unroll
-                for (int c = 0; c < D / 32; c += 2) {         // two TMEM loads per wait
-                    uint32_t rr[2][32];
-                    tmem_ld32(tB + lane_base + c * 32, rr[0]);
-                    tmem_ld32(tB + lane_base + c * 32 + 32, rr[1]);
-                    tmem_ld_wait();
-                    if (c + 2 >= D / 32) {
-                        tc_fence_before();
-                        mbar_arrive(&bb.dq_free);         // B may now take dP of the next tile
-                    }
-                    if (qrow < Qn) {
-#pragma unroll
-                        for (int u = 0; u < 2; ++u)
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4)
-                                red_add4(dst + (c + u) * 32 + j, scale * __uint_as_float(rr[u][j]),
-                                         scale * __uint_as_float(rr[u][j + 1]), scale * __uint_as_float(rr[u][j + 2]),
-                                         scale * __uint_as_float(rr[u][j + 3]));
-                    }
+                for (int u = 0; u < 4; ++u) {
+                    const int chunk = c * 4 + u;
+                    *reinterpret_cast<uint4*>(ds_panel + ((chunk ^ (r & 7)) << 4)) =
+                        make_uint4(d2[4 * u], d2[4 * u + 1], d2[4 * u + 2], d2[4 * u + 3]);
                 }
             }
-            // dV rows of this key tile
-            const int64_t x = x0 + r;
-            float* dvr = dv + (x * H + h) * D;
-            const bool aborted = __any_sync(kAll, *(volatile int*)&bb.abort_flag != 0);
-            if (cnt > 0 && ok && !aborted && uniform_wait(&bb.mma_fin, 0)) {
-                tc_fence_after();
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bb.ds_full);
+        }
+        // dK (scaled) and dV rows of this key tile, columns split between the two
+        // halves, once every MMA of the block has completed; zeros if no query sees it
+        const bool aborted = __any_sync(kAll, *(volatile int*)&bb.abort_flag != 0);
+        constexpr int kHalf = D / 2;
+        float* dkr = dk + (x * H + h) * D + hf * kHalf;
+        float* dvr = dv + (x * H + h) * D + hf * kHalf;
+        if (cnt > 0 && ok && !aborted && uniform_wait(&bb.mma_fin, 0)) {
+            tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t rv[32];
-                    tmem_ld32(tdV + lane_base + c * 32, rv);
-                    tmem_ld_wait();
+            for (int c = 0; c < kHalf / 32; ++c) {
+                uint32_t rk[32], rv[32];
+                tmem_ld32(tdK + lane_base + hf * kHalf + c * 32, rk);
+                tmem_ld32(tdV + lane_base + hf * kHalf + c * 32, rv);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        __stcs(reinterpret_cast<float4*>(dvr + c * 32 + j),
-                               make_float4(__uint_as_float(rv[j]), __uint_as_float(rv[j + 1]),
-                                           __uint_as_float(rv[j + 2]), __uint_as_float(rv[j + 3])));
+                for (int j = 0; j < 32; j += 4) {
+                    __stcs(reinterpret_cast<float4*>(dkr + c * 32 + j),
+                           make_float4(scale * __uint_as_float(rk[j]), scale * __uint_as_float(rk[j + 1]),
+                                       scale * __uint_as_float(rk[j + 2]), scale * __uint_as_float(rk[j + 3])));
+                    __stcs(reinterpret_cast<float4*>(dvr + c * 32 + j),
+                           make_float4(__uint_as_float(rv[j]), __uint_as_float(rv[j + 1]), __uint_as_float(rv[j + 2]),
+                                       __uint_as_float(rv[j + 3])));
                 }
-            } else if (cnt == 0) {
+            }
+        } else if (cnt == 0) {
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int j = 0; j < D; j += 4) __stcs(reinterpret_cast<float4*>(dvr + j), make_float4(0.f, 0.f, 0.f, 0.f));
+            for (int j = 0; j < kHalf; j += 4) {
+                __stcs(reinterpret_cast<float4*>(dkr + j), z);
+                __stcs(reinterpret_cast<float4*>(dvr + j), z);
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kKvMma) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
 }
+
+// =================================================================== dQ
+
+constexpr int kQThreads = 320;                       // compute warps 0-7, MMA 8, TMA 9
+constexpr int kQMma = 8, kQTma = 9;
+constexpr int kKStages = 3, kVStages = 2;
+
+template <int D>
+struct QTiles {                                      // 1024-byte aligned
+    __nv_bfloat16 q[D / 64][BM * 64];
+    __nv_bfloat16 dO[D / 64][BM * 64];
+    __nv_bfloat16 k[kKStages][D / 64][BN * 64];
+    __nv_bfloat16 v[kVStages][D / 64][BN * 64];
+};
+
+struct QMeta {
+    float lse2[BM];
+    float D[BM];
+};
+
+struct QBars {
+    uint64_t q_full, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+    uint64_t s_full[2], dp_full, ds_full, mma_fin, stuck;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+template <int D>
+struct QSmem {
+    QTiles<D> t;
+    QMeta meta;
+    QBars b;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kQThreads, 1)
+attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+                      const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                      const float* __restrict__ lse2_hm, const float* __restrict__ D_hm, int64_t Qp,
+                      const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int64_t Qn, int H,
+                      int64_t S, int m, int P, float scale, float scale_log2, const int4* __restrict__ qtb,
+                      skv::RankCSR csr, float* __restrict__ dq, int* status, long long wait_limit) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t base_s = smem_u32(smem_raw);
+    const uint32_t pad = ((base_s + 1023u) & ~1023u) - base_s;
+    if (pad + sizeof(QSmem<D>) > (size_t)kSmemMax) {
+        if (threadIdx.x == 0) skv::raise_status(status, SKV_ERR_UNSUPPORTED);
+        return;
+    }
+    QSmem<D>& sm = *reinterpret_cast<QSmem<D>*>(smem_raw + pad);
+    QTiles<D>& tl = sm.t;
+    QBars& bb = sm.b;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qt = blockIdx.x, h = blockIdx.y;
+    constexpr int NP = D / 64;
+    constexpr uint32_t kTile = BM * D * 2;
+    const bool stuck_test = wait_limit < 0;
+    if (stuck_test) wait_limit = -wait_limit;
+    int4 bnd = qtb[qt];
+    if (*(volatile int*)status == SKV_ERR_TIMEOUT) bnd.y = bnd.x;   // launch already void: no tiles
+    TileIter it;
+    it.init(csr, 0, P, m, bnd.x, bnd.y);             // every rank's chunks: dq = sum_p dq^(p)
+
+    if (tid == 0) {
+        mbar_init(&bb.q_full, 1);
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(&bb.k_full[i], 1);
+            mbar_init(&bb.k_empty[i], 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(&bb.v_full[i], 1);
+            mbar_init(&bb.v_empty[i], 1);
+        }
+        mbar_init(&bb.s_full[0], 1);
+        mbar_init(&bb.s_full[1], 1);
+        mbar_init(&bb.dp_full, 1);
+        mbar_init(&bb.ds_full, 256);
+        mbar_init(&bb.mma_fin, 1);
+        mbar_init(&bb.stuck, 1);
+        bb.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kQMma) {
+        tmem_alloc(&bb.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bb.tmem_base;
+    const uint32_t tS = tmem, tP = tmem + 256, tQ = tmem + 384;   // S double buffer, dP, dQ accumulator
+    auto abort_now = [&]() {
+        atomicExch(&bb.abort_flag, 1);
+        skv::raise_status(status, SKV_ERR_TIMEOUT);
+    };
+
+    if (warp == kQTma) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int n = 0;       // key tiles whose K load was issued
+            int nv = 0;      // key tiles whose V load was issued
+            int64_t x0;
+            bool any = false;
+            while (it.next(x0)) {
+                if (!any) {
+                    prefetch_tensormap(&map_k);
+                    prefetch_tensormap(&map_v);
+                    mbar_arrive_expect_tx(&bb.q_full, 2 * kTile + 2 * BM * 4);
+                    for (int c = 0; c < NP; ++c) {
+                        tma_load_2d(tl.q[c], &map_q, &bb.q_full, h * D + c * 64, qt * BM);
+                        tma_load_2d(tl.dO[c], &map_do, &bb.q_full, h * D + c * 64, qt * BM);
+                    }
+                    bulk_load(sm.meta.lse2, lse2_hm + int64_t(h) * Qp + int64_t(qt) * BM, BM * 4, &bb.q_full);
+                    bulk_load(sm.meta.D, D_hm + int64_t(h) * Qp + int64_t(qt) * BM, BM * 4, &bb.q_full);
+                    any = true;
+                }
+                const int ks = n % kKStages, vs = n % kVStages;
+                if (n >= kKStages &&
+                    !mbar_wait(&bb.k_empty[ks], ((n - kKStages) / kKStages) & 1, wait_limit, &bb.abort_flag)) {
+                    abort_now();
+                    break;
+                }
+                if (*(volatile int*)&bb.abort_flag) break;
+                mbar_arrive_expect_tx(&bb.k_full[ks], kTile);
+                for (int c = 0; c < NP; ++c) tma_load_2d(tl.k[ks][c], &map_k, &bb.k_full[ks], h * D + c * 64, (int)x0);
+                ++n;
+                if (n - 1 >= kVStages &&
+                    !mbar_wait(&bb.v_empty[vs], ((n - 1 - kVStages) / kVStages) & 1, wait_limit, &bb.abort_flag)) {
+                    abort_now();
+                    break;
+                }
+                mbar_arrive_expect_tx(&bb.v_full[vs], kTile);
+                for (int c = 0; c < NP; ++c) tma_load_2d(tl.v[vs][c], &map_v, &bb.v_full[vs], h * D + c * 64, (int)x0);
+                ++nv;
+            }
+            // every copy issued has landed before the block exits
+            if (any) mbar_wait(&bb.q_full, 0, kTeardownWait);
+            for (int st = 0; st < kKStages && st < n; ++st) {
+                const int last = st + ((n - 1 - st) / kKStages) * kKStages;
+                mbar_wait(&bb.k_full[st], (last / kKStages) & 1, kTeardownWait);
+            }
+            for (int st = 0; st < kVStages && st < nv; ++st) {
+                const int last = st + ((nv - 1 - st) / kVStages) * kVStages;
+                mbar_wait(&bb.v_full[st], (last / kVStages) & 1, kTeardownWait);
+            }
+        }
+    } else if (warp == kQMma) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);    // M = queries, N = keys, K = d
+            constexpr uint32_t idQ = idesc_bf16_f32(BM, D, 0, 1);     // M = queries, N = d, K = keys
+            int T = 0;
+            {
+                TileIter cnt = it;
+                int64_t x0;
+                while (cnt.next(x0)) ++T;
+            }
+            bool issued = false;
+            bool ok = T > 0;
+            if (ok && stuck_test && !mbar_wait(&bb.stuck, 0, wait_limit, &bb.abort_flag)) ok = false;
+            if (ok) ok = mbar_wait(&bb.q_full, 0, wait_limit, &bb.abort_flag);
+            auto issue_s = [&](int n) -> bool {            // S_n = Q K_n^T -> S[n&1]
+                const int ks = n % kKStages;
+                if (!mbar_wait(&bb.k_full[ks], (n / kKStages) & 1, wait_limit, &bb.abort_flag)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    mma_ss(tS + (n & 1) * 128, smem_desc(smem_u32(tl.q[kk >> 2]) + off, 16, 1024),
+                           smem_desc(smem_u32(tl.k[ks][kk >> 2]) + off, 16, 1024), idS, kk > 0);
+                }
+                mma_commit(&bb.s_full[n & 1]);
+                issued = true;
+                return true;
+            };
+            auto issue_dp = [&](int n) -> bool {           // dP_n = dO V_n^T -> dP
+                const int vs = n % kVStages;
+                if (!mbar_wait(&bb.v_full[vs], (n / kVStages) & 1, wait_limit, &bb.abort_flag)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    mma_ss(tP, smem_desc(smem_u32(tl.dO[kk >> 2]) + off, 16, 1024),
+                           smem_desc(smem_u32(tl.v[vs][kk >> 2]) + off, 16, 1024), idS, kk > 0);
+                }
+                mma_commit(&bb.dp_full);
+                mma_commit(&bb.v_empty[vs]);
+                issued = true;
+                return true;
+            };
+            if (ok) ok = issue_s(0) && issue_dp(0) && (T < 2 || issue_s(1));
+            for (int n = 0; ok && n < T; ++n) {
+                if (!mbar_wait(&bb.ds_full, n & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                // dQ += dS_n K_n: bf16 dS of key columns [64h, 64h+64) sits in TMEM columns
+                // [64h, 64h+32) of S[n&1]
+                const int ks = n % kKStages;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tQ, tS + (n & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
+                           smem_desc(smem_u32(tl.k[ks][0]) + kk * 2048, BN * 128, 1024), idQ,
+                           (n > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bb.k_empty[ks]);
+                // dP held dP_n, which the compute warps finished reading before ds_full
+                if (n + 1 < T && !issue_dp(n + 1)) { ok = false; break; }
+                // S_{n+2} overwrites S[n&1] right behind the dQ MMA that reads dS_n from it
+                if (n + 2 < T && !issue_s(n + 2)) { ok = false; break; }
+            }
+            if (!ok && T > 0) abort_now();
+            if (issued) {
+                mma_commit(&bb.mma_fin);
+                if (!mbar_wait(&bb.mma_fin, 0, kTeardownWait)) skv::raise_status(status, SKV_ERR_TIMEOUT);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ compute warps 0-7
+        // warp w owns query rows (TMEM lanes) of quadrant w%4 and key columns
+        // [64*hf, 64*hf+64) with hf = w/4
+        constexpr unsigned kAll = 0xffffffffu;
+        const int quad = warp & 3, hf = warp >> 2;
+        const uint32_t lane_base = uint32_t(quad * 32) << 16;
+        const int r = quad * 32 + lane;
+        const int64_t row = int64_t(qt) * BM + r;
+        const bool live = row < Qn;
+        int64_t rlo = 0, rhi = 0;
+        if (live) skv::block_window(s, a, (int)(row / B), S, rlo, rhi);
+        bool ok = true;
+        auto uniform_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+            const bool got = mbar_wait_warp(bar, parity, wait_limit, &bb.abort_flag);
+            if (!got && lane == 0) abort_now();
+            return got;
+        };
+        float l2 = INFINITY, Dr = 0.f;
+        int64_t x0;
+        int n = 0;
+        while (it.next(x0)) {
+            if (n == 0) {
+                if (!uniform_wait(&bb.q_full, 0)) { ok = false; break; }
+                l2 = sm.meta.lse2[r];
+                Dr = sm.meta.D[r];
+            }
+            if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
+            const bool full = (x0 >= bnd.z) && (x0 + BN <= bnd.w);
+            const uint32_t sbuf = tS + (n & 1) * 128;
+            if (!uniform_wait(&bb.s_full[n & 1], (n >> 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t sraw[2][32];
+            tmem_ld32(sbuf + lane_base + hf * 64, sraw[0]);
+            tmem_ld32(sbuf + lane_base + hf * 64 + 32, sraw[1]);
+            tmem_ld_wait();
+            float pr[2][32];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t keep = 0xffffffffu;              // key columns this row sees
+                if (!full) {                              // boundary tile only
+                    const int64_t xc = x0 + hf * 64 + c * 32;
+                    const int64_t lo = rlo - xc, hi = rhi - xc;   // window relative to the chunk
+                    keep = 0u;
+                    if (hi > 0 && lo < 32) {
+                        const int b0 = lo > 0 ? (int)lo : 0, b1 = hi < 32 ? (int)hi : 32;
+                        keep = (b1 >= 32 ? 0xffffffffu : ((1u << b1) - 1u)) & ~((1u << b0) - 1u);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    pr[c][j] = ((keep >> j) & 1u) ? ex2(fmaf(__uint_as_float(sraw[c][j]), scale_log2, -l2)) : 0.f;
+            }
+            if (!uniform_wait(&bb.dp_full, n & 1)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t draw[2][32];
+            tmem_ld32(tP + lane_base + hf * 64, draw[0]);
+            tmem_ld32(tP + lane_base + hf * 64 + 32, draw[1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    pk[j] = pack_bf16(pr[c][2 * j] * (__uint_as_float(draw[c][2 * j]) - Dr),
+                                      pr[c][2 * j + 1] * (__uint_as_float(draw[c][2 * j + 1]) - Dr));
+                // bf16 dS of key columns [64hf + 32c, +32) -> TMEM columns [64hf + 16c, +16)
+                // of this S buffer: inside this warp's half, over columns read already
+                tmem_st16(sbuf + lane_base + hf * 64 + c * 16, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bb.ds_full);
+            ++n;
+        }
+        // dq rows (scaled), columns split between the two halves; zeros if no key
+        const bool aborted = __any_sync(kAll, *(volatile int*)&bb.abort_flag != 0);
+        constexpr int kHalf = D / 2;
+        float* dqr = dq + (row * H + h) * D + hf * kHalf;
+        if (n > 0 && ok && !aborted && uniform_wait(&bb.mma_fin, 0)) {
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < kHalf / 32; ++c) {
+                uint32_t rq[32];
+                tmem_ld32(tQ + lane_base + hf * kHalf + c * 32, rq);
+                tmem_ld_wait();
+                if (live) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        __stcs(reinterpret_cast<float4*>(dqr + c * 32 + j),
+                               make_float4(scale * __uint_as_float(rq[j]), scale * __uint_as_float(rq[j + 1]),
+                                           scale * __uint_as_float(rq[j + 2]), scale * __uint_as_float(rq[j + 3])));
+                }
+            }
+        } else if (n == 0 && live) {
+#pragma unroll
+            for (int j = 0; j < kHalf; j += 4) __stcs(reinterpret_cast<float4*>(dqr + j), make_float4(0.f, 0.f, 0.f, 0.f));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kQMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ============================================================== host side
 
 struct BwdScratch {
     int4* qtb;
@@ -511,8 +771,8 @@ size_t scratch_layout(const skv_problem& pb, BwdScratch* w, char* base) {
 
 template <int D>
 skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const void* v, const void* dO,
-                      const float* lse2_hm, const float* D_hm, float* dq, float* dk, float* dv, void* scratch,
-                      const skv_host::Ctx& c) {
+                      const float* lse2_hm, const float* D_hm, skv::RankCSR csr, float* dq, float* dk, float* dv,
+                      void* scratch, const skv_host::Ctx& c) {
     const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
     const int n_qt = (int)((Qn + BM - 1) / BM);
     const int64_t Qp = int64_t(n_qt) * BM;
@@ -528,14 +788,23 @@ skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const
     if (!make_map(&mq, q, Qn, cols) || !make_map(&mdo, dO, Qn, cols) || !make_map(&mk, k, pb.S, cols) ||
         !make_map(&mv, v, pb.S, cols))
         return SKV_ERR_CUDA;
-    SKV_CUDA_CHECK(cudaMemsetAsync(dq, 0, size_t(Qn) * cols * sizeof(float), c.stream));
-    auto kern = attn_bwd_tc_kernel<D>;
-    SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax));
-    const dim3 grid((unsigned)n_kv, (unsigned)pb.n_heads);
-    kern<<<grid, kBwdThreads, kSmemMax, c.stream>>>(mq, mdo, mk, mv, lse2_hm, D_hm, Qp, pb.s, pb.a, pb.B, Qn,
-                                                    pb.n_heads, pb.S, pb.scale, pb.scale * 1.4426950408889634f, w.qtb,
-                                                    w.cnt, w.list, n_qt, dq, dk, dv, c.status, c.wait_limit);
-    SKV_LAUNCHED();
+    const float scale_log2 = pb.scale * 1.4426950408889634f;
+    {
+        auto kern = attn_bwd_dkdv_tc_kernel<D>;
+        SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax));
+        kern<<<dim3((unsigned)n_kv, (unsigned)pb.n_heads), kKvThreads, kSmemMax, c.stream>>>(
+            mq, mdo, mk, mv, lse2_hm, D_hm, Qp, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.scale, scale_log2, w.qtb,
+            w.cnt, w.list, n_qt, dk, dv, c.status, c.wait_limit);
+        SKV_LAUNCHED();
+    }
+    {
+        auto kern = attn_bwd_dq_tc_kernel<D>;
+        SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax));
+        kern<<<dim3((unsigned)n_qt, (unsigned)pb.n_heads), kQThreads, kSmemMax, c.stream>>>(
+            mq, mdo, mk, mv, lse2_hm, D_hm, Qp, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.m, pb.P, pb.scale,
+            scale_log2, w.qtb, csr, dq, c.status, c.wait_limit);
+        SKV_LAUNCHED();
+    }
     return SKV_OK;
 }
 
@@ -553,10 +822,10 @@ size_t bwd_scratch_bytes(const skv_problem& pb) {
 }
 
 skv_status launch_attn_bwd_tc(const skv_problem& pb, const void* q, const void* k, const void* v, const void* dO,
-                              const float* lse2, const float* D, skv::RankCSR, float* dq, float* dk, float* dv,
+                              const float* lse2, const float* D, skv::RankCSR csr, float* dq, float* dk, float* dv,
                               void* scratch, const skv_host::Ctx& c) {
-    if (pb.head_dim == 128) return launch_bwd<128>(pb, q, k, v, dO, lse2, D, dq, dk, dv, scratch, c);
-    return launch_bwd<64>(pb, q, k, v, dO, lse2, D, dq, dk, dv, scratch, c);
+    if (pb.head_dim == 128) return launch_bwd<128>(pb, q, k, v, dO, lse2, D, csr, dq, dk, dv, scratch, c);
+    return launch_bwd<64>(pb, q, k, v, dO, lse2, D, csr, dq, dk, dv, scratch, c);
 }
 
 }  // namespace skv_tc

@@ -48,39 +48,6 @@ struct __align__(1024) FwdSmem {
     int abort_flag;
 };
 
-// Walks the 128-key tiles of rank p's chunks that intersect [lo, hi).  Every
-// role runs its own copy and sees the same sequence.
-struct TileIter {
-    const int32_t* list;
-    int ci, ce, m;
-    int64_t x, xe, lo, hi;
-    __device__ __forceinline__ void init(skv::RankCSR csr, int p, int m_, int64_t lo_, int64_t hi_) {
-        list = csr.list;
-        ci = csr.ptr[p];
-        ce = csr.ptr[p + 1];
-        m = m_;
-        lo = lo_;
-        hi = hi_;
-        x = 0;
-        xe = 0;
-    }
-    __device__ __forceinline__ bool next(int64_t& x0) {
-        while (x >= xe) {
-            if (ci >= ce) return false;
-            const int64_t cl = int64_t(list[ci++]) * m;
-            const int64_t a0 = cl > lo ? cl : lo;
-            const int64_t a1 = (cl + m) < hi ? (cl + m) : hi;
-            if (a0 < a1) {
-                x = a0 & ~int64_t(BN - 1);
-                xe = a1;
-            }
-        }
-        x0 = x;
-        x += BN;
-        return true;
-    }
-};
-
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -132,7 +99,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     const uint32_t tS = tmem, tO = tmem + 256, tP = tmem + 384;
 
     TileIter it;
-    it.init(csr, p, m, tb.lo, tb.hi);
+    it.init(csr, p, p + 1, m, tb.lo, tb.hi);
 
     if (warp == 5) {
         // ------------------------------------------------------------ producer

@@ -39,6 +39,40 @@ __device__ __forceinline__ TileBounds tile_bounds(const int32_t* s, const int32_
     return tb;
 }
 
+// Walks the 128-key tiles of rank p's chunks that intersect [lo, hi).  Every
+// role runs its own copy and sees the same sequence.
+struct TileIter {
+    const int32_t* list;
+    int ci, ce, m;
+    int64_t x, xe, lo, hi;
+    // ranks [p0, p1): the CSR list is rank-major, ascending inside a rank
+    __device__ __forceinline__ void init(skv::RankCSR csr, int p0, int p1, int m_, int64_t lo_, int64_t hi_) {
+        list = csr.list;
+        ci = csr.ptr[p0];
+        ce = csr.ptr[p1];
+        m = m_;
+        lo = lo_;
+        hi = hi_;
+        x = 0;
+        xe = 0;
+    }
+    __device__ __forceinline__ bool next(int64_t& x0) {
+        while (x >= xe) {
+            if (ci >= ce) return false;
+            const int64_t cl = int64_t(list[ci++]) * m;
+            const int64_t a0 = cl > lo ? cl : lo;
+            const int64_t a1 = (cl + m) < hi ? (cl + m) : hi;
+            if (a0 < a1) {
+                x = a0 & ~int64_t(BN - 1);
+                xe = a1;
+            }
+        }
+        x0 = x;
+        x += BN;
+        return true;
+    }
+};
+
 
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
