@@ -11,9 +11,10 @@
 //    tile-skip list (built by qtile_bounds_kernel / kv_list_kernel; masked-out
 //    query tiles are never loaded).  Per query tile t:
 //      S^T = K Q_t^T, dP^T = V dO_t^T (SS) -> TMEM A, B
-//      eight warps: P^T = exp2(S^T scale log2e - l2) (bf16 -> TMEM A),
-//                   dS^T = P^T (dP^T - D) (bf16 -> swizzled shared memory)
-//      dV += P^T dO_t (TS), dK += dS^T Q_t (SS)
+//      eight warps: P^T = exp2(S^T scale log2e - l2), dS^T = P^T (dP^T - D),
+//                   both bf16 -> TMEM B over the dP^T they have read
+//      dV += P^T dO_t, dK += dS^T Q_t (TS: A operands from TMEM); S of the next
+//      tile is issued as soon as S^T has been read, so it overlaps the exponentials
 //  * attn_bwd_dq_tc_kernel -- query-stationary.  One thread block owns a
 //    128-row query tile and a head and walks, rank by rank, the key tiles of
 //    every rank's chunks that meet the tile's windows: dq = sum_p dq^(p)
@@ -90,7 +91,6 @@ struct KvTiles {                                     // 1024-byte aligned (128-b
     __nv_bfloat16 v[D / 64][BN * 64];
     __nv_bfloat16 q[2][D / 64][BM * 64];
     __nv_bfloat16 dO[2][D / 64][BM * 64];
-    __nv_bfloat16 ds[2][BN * 64];                    // dS^T [key][q], two 64-query panels
 };
 
 struct KvMeta {                                      // per query tile, loaded with its Q/dO stage
@@ -102,7 +102,7 @@ struct KvMeta {                                      // per query tile, loaded w
 };
 
 struct KvBars {
-    uint64_t kv_full, qd_full[2], qd_empty[2], s_full, dp_full, ds_full, mma_fin;
+    uint64_t kv_full, qd_full[2], qd_empty[2], s_full, s_read, dp_full, ds_full, mma_fin;
     uint64_t stuck;                                  // never completed: target of the forced-timeout test mode
     uint32_t tmem_base;
     int abort_flag;
@@ -155,6 +155,7 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             mbar_init(&bb.qd_empty[i], 1);
         }
         mbar_init(&bb.s_full, 1);
+        mbar_init(&bb.s_read, 256);
         mbar_init(&bb.dp_full, 1);
         mbar_init(&bb.ds_full, 256);
         mbar_init(&bb.mma_fin, 1);
@@ -246,20 +247,14 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 issue_dp(0);
                 issued = true;
             }
+            // per query tile t:
+            //   [S_t read]  S_{t+1} -> A   (overlaps the compute warps' P_t / dS_t)
+            //   [dS_t done] dV_t += P_t dO_t, dK_t += dS_t Q_t (P_t, dS_t bf16 in B over the
+            //               read dP_t), then dP_{t+1} -> B behind them in issue order
             for (int t = 0; ok && t < cnt; ++t) {
                 const int st = t & 1;
-                if (!mbar_wait(&bb.ds_full, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                // dV += P^T dO.  bf16 P^T of query columns [64h, 64h+64) sits in TMEM
-                // columns [64h, 64h+32) of A (each half of the compute warps writes inside its half)
-#pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts(tdV, tA + (kk >> 2) * 64 + (kk & 3) * 8,
-                           smem_desc(smem_u32(tl.dO[st][0]) + kk * 2048, BM * 128, 1024), idKV,
-                           (t > 0 || kk > 0) ? 1u : 0u);
-                // S_{t+1} overwrites A right behind the dV MMA that reads P_t from it:
-                // the MMAs of one thread execute in issue order
                 const bool more = t + 1 < cnt;
+                if (!mbar_wait(&bb.s_read, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
                 if (more) {
                     if (!mbar_wait(&bb.qd_full[(t + 1) & 1], ((t + 1) >> 1) & 1, wait_limit, &bb.abort_flag)) {
                         ok = false;
@@ -268,13 +263,22 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                     tc_fence_after();
                     issue_s((t + 1) & 1);
                 }
+                if (!mbar_wait(&bb.ds_full, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                // dV += P^T dO.  bf16 P^T of query columns [64h, 64h+64) sits in TMEM
+                // columns [64h, 64h+32) of B (each half of the compute warps writes inside its half)
 #pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)      // dK += dS^T Q
-                    mma_ss(tdK, smem_desc(smem_u32(tl.ds[kk >> 2]) + (kk & 3) * 32, 16, 1024),
+                for (int kk = 0; kk < BM / 16; ++kk)
+                    mma_ts(tdV, tB + (kk >> 2) * 64 + (kk & 3) * 8,
+                           smem_desc(smem_u32(tl.dO[st][0]) + kk * 2048, BM * 128, 1024), idKV,
+                           (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk)      // dK += dS^T Q (bf16 dS^T in B, after P^T)
+                    mma_ts(tdK, tB + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
                            smem_desc(smem_u32(tl.q[st][0]) + kk * 2048, BM * 128, 1024), idKV,
                            (t > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bb.qd_empty[st]);
-                // B held dP_t, which the compute warps finished reading before ds_full
+                // dP_{t+1} overwrites B right behind the dV and dK MMAs reading P_t, dS_t from it
                 if (more) issue_dp((t + 1) & 1);
             }
             if (!ok) abort_now();
@@ -298,7 +302,6 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             if (!got && lane == 0) abort_now();
             return got;
         };
-        unsigned char* ds_panel = reinterpret_cast<unsigned char*>(&tl.ds[hf][0]) + r * 128;
         for (int t = 0; t < cnt; ++t) {
             const int st = t & 1;
             if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
@@ -309,12 +312,15 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             const bool full = (x0 >= bnd.z) && (x0 + BN <= bnd.w);
             if (!uniform_wait(&bb.s_full, t & 1)) { ok = false; break; }
             tc_fence_after();
-            // both 32-column chunks of S^T are loaded before one wait; P^T is kept as
-            // the bf16 pairs the dV MMA consumes and dS^T is formed from those values
+            // both 32-column chunks of S^T are loaded before one wait; A is then free
+            // for S of the next tile.  P^T is kept as the bf16 pairs the dV MMA
+            // consumes and dS^T is formed from those values.
             uint32_t sraw[2][32];
             tmem_ld32(tA + lane_base + hf * 64, sraw[0]);
             tmem_ld32(tA + lane_base + hf * 64 + 32, sraw[1]);
             tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&bb.s_read);
             uint32_t pk[2][16];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -345,9 +351,6 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                     pk[c][2 * j4] = pack_bf16(pv[0], pv[1]);
                     pk[c][2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
                 }
-                // bf16 pairs of these 32 columns -> TMEM columns [64hf + 16c, +16): inside
-                // this warp's own half, over S^T columns it has read already
-                tmem_st16(tA + lane_base + hf * 64 + c * 16, pk[c]);
             }
             if (!uniform_wait(&bb.dp_full, t & 1)) { ok = false; break; }
             tc_fence_after();
@@ -355,31 +358,30 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             tmem_ld32(tB + lane_base + hf * 64, draw[0]);
             tmem_ld32(tB + lane_base + hf * 64 + 32, draw[1]);
             tmem_ld_wait();
+            // bf16 P^T of columns [64hf + 32c, +32) -> TMEM B columns [64hf + 16c, +16):
+            // inside this warp's half, over dP^T columns it has just read
+            tmem_st16(tB + lane_base + hf * 64, pk[0]);
+            tmem_st16(tB + lane_base + hf * 64 + 16, pk[1]);
+            uint32_t d2[2][16];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int col0 = hf * 64 + c * 32;
-                uint32_t d2[16];
                 const float4* d4 = reinterpret_cast<const float4*>(md.D + col0);
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const float4 dd = d4[j4];
                     const float2 p01 = unpack_bf16(pk[c][2 * j4]);
                     const float2 p23 = unpack_bf16(pk[c][2 * j4 + 1]);
-                    d2[2 * j4] = pack_bf16(p01.x * (__uint_as_float(draw[c][4 * j4]) - dd.x),
-                                           p01.y * (__uint_as_float(draw[c][4 * j4 + 1]) - dd.y));
-                    d2[2 * j4 + 1] = pack_bf16(p23.x * (__uint_as_float(draw[c][4 * j4 + 2]) - dd.z),
-                                               p23.y * (__uint_as_float(draw[c][4 * j4 + 3]) - dd.w));
-                }
-                // query columns [64hf + 32c, +32) = panel hf, 16-byte chunks 4c .. 4c+3
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int chunk = c * 4 + u;
-                    *reinterpret_cast<uint4*>(ds_panel + ((chunk ^ (r & 7)) << 4)) =
-                        make_uint4(d2[4 * u], d2[4 * u + 1], d2[4 * u + 2], d2[4 * u + 3]);
+                    d2[c][2 * j4] = pack_bf16(p01.x * (__uint_as_float(draw[c][4 * j4]) - dd.x),
+                                              p01.y * (__uint_as_float(draw[c][4 * j4 + 1]) - dd.y));
+                    d2[c][2 * j4 + 1] = pack_bf16(p23.x * (__uint_as_float(draw[c][4 * j4 + 2]) - dd.z),
+                                                  p23.y * (__uint_as_float(draw[c][4 * j4 + 3]) - dd.w));
                 }
             }
+            // bf16 dS^T of columns [64hf + 32c, +32) -> TMEM B columns [64hf + 32 + 16c, +16)
+            tmem_st16(tB + lane_base + hf * 64 + 32, d2[0]);
+            tmem_st16(tB + lane_base + hf * 64 + 48, d2[1]);
             tmem_st_wait();
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bb.ds_full);
         }
