@@ -19,6 +19,7 @@ import os
 os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
 
 import argparse
+import ctypes
 import json
 import statistics
 import subprocess
@@ -238,6 +239,8 @@ def run_ours(args):
             skv.attn_bwd(prob, q, k, v, o, lse, dO, roc, dq, dk, dv, ws_b)
         if ev: ev[4].record()
 
+    kt_names = ["attn_fwd_tc_kernel", "lse_merge_kernel", "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel"]
+    kt_buf = (ctypes.c_float * 4)()
     for _ in range(args.warmup):
         path()
     torch.cuda.synchronize()
@@ -277,6 +280,18 @@ def run_ours(args):
         ms = float(tt.item())
     if skv.stream_status() != 0:
         raise RuntimeError("device status set during the timed region")
+    # per-kernel durations: the library's own CUDA events on the launching
+    # stream, read after each step of a separate pass of the same steps
+    kt_ms = [[] for _ in kt_names]
+    lib.skv_set_kernel_timing(1)
+    for t in range(max(3, min(args.steps, 5))):
+        path()
+        if lib.skv_kernel_times(kt_buf, 4) == 0:
+            for i in range(4):
+                if kt_buf[i] >= 0:
+                    kt_ms[i].append(kt_buf[i])
+    lib.skv_set_kernel_timing(0)
+    torch.cuda.synchronize()
 
     pairs = useful_pairs_per_head(inp.s, inp.a, w.B) * H
     fwd_flops = 4.0 * d * pairs
@@ -290,17 +305,27 @@ def run_ours(args):
     out_b = 2 if tdt == torch.bfloat16 else 4
     merge_bytes = P * Q * H * 4 + finite * d * 4 + Q * H * (d * out_b + 4)
     merge_gbs = merge_bytes / (ph["merge"] * 1e-3) / 1e9
-    attn = {"fwd": (fwd_flops, ph["fwd"])}
-    if w.backward:
-        attn["bwd"] = (bwd_flops, ph["bwd"])
-    dom = max(attn, key=lambda x: attn[x][1])
-    dom_tf = attn[dom][0] / (attn[dom][1] * 1e-3) / 1e12
+    # credited (useful) FLOP of each main kernel per launch: forward 4d per pair;
+    # the backward's 8d per pair (dV, dP, dQ, dK) is credited 6d to the dK/dV
+    # kernel (dV, dP, dK) and 2d to the dQ kernel (dQ; its S and dP are recompute)
+    credit = {"attn_fwd_tc_kernel": 4.0 * d * pairs, "attn_bwd_dkdv_tc_kernel": 6.0 * d * pairs,
+              "attn_bwd_dq_tc_kernel": 2.0 * d * pairs}
+    kernels = {}
+    for i, nm in enumerate(kt_names):
+        if kt_ms[i]:
+            km = statistics.mean(kt_ms[i])
+            kernels[nm] = {"ms": km}
+            if nm in credit:
+                kernels[nm]["useful_tflops"] = credit[nm] / (km * 1e-3) / 1e12
+    tensor_k = {k: v for k, v in kernels.items() if k in credit}
+    dom = max(tensor_k, key=lambda k: tensor_k[k]["ms"]) if tensor_k else None
+    dom_tf = tensor_k[dom]["useful_tflops"] if dom else 0.0
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
+    if dom and os.path.exists(tr_path):
         with open(tr_path) as f:
-            tr = json.load(f).get(w.name, {}).get(dom)
-        traffic = tr if tr else None
+            per_pair = json.load(f).get(dom, {}).get("dram_bytes_per_useful_pair_head")
+        traffic = per_pair * pairs if per_pair else None
 
     # end to end through the public API with host buffers (pinned), copies inside
     e2e = None
@@ -359,9 +384,10 @@ def run_ours(args):
             "useful_tflop_per_step": step_flops / 1e12,
             "merge": {"gbs": merge_gbs, "bytes": merge_bytes, "frac_of_hbm": merge_gbs / hbm,
                       "peak_gbs": hbm, "peak_kind": pk_kind},
-            "roofline": {"kernel": f"attn_{dom}", "bound": "tensor", "achieved": dom_tf,
+            "roofline": {"kernel": dom, "bound": "tensor", "achieved": dom_tf,
                          "peak": sustained, "unit": "TFLOP/s", "frac": dom_tf / sustained,
                          "peak_kind": f"{pk_kind} sustained bf16", "traffic": traffic},
+            "kernels": kernels,
             "gpu_launches": int(launches),
             "clocks": clk,
             "e2e": e2e,

@@ -249,6 +249,18 @@ SKV_API skv_status skv_set_wait_limit(int64_t limit);
  */
 SKV_API uint64_t skv_launch_count(void);
 
+/*
+ * Measurement hook.  skv_set_kernel_timing(1) makes the library record a
+ * CUDA event pair on the launching stream around each of its main kernels:
+ * slot 0 the forward attention kernel, 1 the LSE merge, 2 the backward dK/dV
+ * kernel, 3 the backward dQ kernel (tensor-core path).  skv_kernel_times
+ * waits for the last recorded pair of each of the first n slots and writes
+ * its duration in milliseconds (-1 where nothing was recorded since the
+ * previous read).  Off by default; the events are created on first use.
+ */
+SKV_API skv_status skv_set_kernel_timing(int enable);
+SKV_API skv_status skv_kernel_times(float* ms, int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,6 +28,8 @@ SIGNATURES = {
     "skv_status_str": (ctypes.c_char_p, [c_int]),
     "skv_set_wait_limit": (c_int, [c_int64]),
     "skv_launch_count": (ctypes.c_uint64, []),
+    "skv_set_kernel_timing": (c_int, [c_int]),
+    "skv_kernel_times": (c_int, [c_void_p, c_int]),
     "skv_attn_fwd_static": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_void_p]),
 }

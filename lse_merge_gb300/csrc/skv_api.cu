@@ -112,6 +112,25 @@ namespace skv_host {
 
 void note_launch(int n) { g_launches.fetch_add(uint64_t(n), std::memory_order_relaxed); }
 
+namespace {
+bool g_timing = false;
+cudaEvent_t g_ev[kTimeSlots][2] = {};
+bool g_ev_live[kTimeSlots] = {};
+}  // namespace
+
+void timer_begin(int slot, cudaStream_t stream) {
+    if (!g_timing || slot < 0 || slot >= kTimeSlots) return;
+    for (int i = 0; i < 2; ++i)
+        if (!g_ev[slot][i] && cudaEventCreate(&g_ev[slot][i]) != cudaSuccess) return;
+    cudaEventRecord(g_ev[slot][0], stream);
+}
+
+void timer_end(int slot, cudaStream_t stream) {
+    if (!g_timing || slot < 0 || slot >= kTimeSlots || !g_ev[slot][1]) return;
+    cudaEventRecord(g_ev[slot][1], stream);
+    g_ev_live[slot] = true;
+}
+
 skv_status get_ctx(void* stream, Ctx& ctx) {
     int dev = 0;
     SKV_CUDA_CHECK(cudaGetDevice(&dev));
@@ -298,6 +317,24 @@ const char* skv_status_str(skv_status s) {
 }
 
 uint64_t skv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+skv_status skv_set_kernel_timing(int enable) {
+    skv_host::g_timing = enable != 0;
+    return SKV_OK;
+}
+
+skv_status skv_kernel_times(float* ms, int n) {
+    if (!ms || n < 0) return SKV_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        ms[i] = -1.f;
+        if (i >= skv_host::kTimeSlots || !skv_host::g_ev_live[i]) continue;
+        if (cudaEventSynchronize(skv_host::g_ev[i][1]) != cudaSuccess) return SKV_ERR_CUDA;
+        if (cudaEventElapsedTime(&ms[i], skv_host::g_ev[i][0], skv_host::g_ev[i][1]) != cudaSuccess)
+            return SKV_ERR_CUDA;
+        skv_host::g_ev_live[i] = false;
+    }
+    return SKV_OK;
+}
 
 skv_status skv_set_wait_limit(int64_t limit) {
     std::lock_guard<std::mutex> lk(g_mu);

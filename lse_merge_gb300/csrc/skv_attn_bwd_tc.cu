@@ -794,17 +794,21 @@ skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const
     {
         auto kern = attn_bwd_dkdv_tc_kernel<D>;
         SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax));
+        skv_host::timer_begin(skv_host::kTimeBwdKV, c.stream);
         kern<<<dim3((unsigned)n_kv, (unsigned)pb.n_heads), kKvThreads, kSmemMax, c.stream>>>(
             mq, mdo, mk, mv, lse2_hm, D_hm, Qp, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.scale, scale_log2, w.qtb,
             w.cnt, w.list, n_qt, dk, dv, c.status, c.wait_limit);
+        skv_host::timer_end(skv_host::kTimeBwdKV, c.stream);
         SKV_LAUNCHED();
     }
     {
         auto kern = attn_bwd_dq_tc_kernel<D>;
         SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax));
+        skv_host::timer_begin(skv_host::kTimeBwdQ, c.stream);
         kern<<<dim3((unsigned)n_qt, (unsigned)pb.n_heads), kQThreads, kSmemMax, c.stream>>>(
             mq, mdo, mk, mv, lse2_hm, D_hm, Qp, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.m, pb.P, pb.scale,
             scale_log2, w.qtb, csr, dq, c.status, c.wait_limit);
+        skv_host::timer_end(skv_host::kTimeBwdQ, c.stream);
         SKV_LAUNCHED();
     }
     return SKV_OK;

@@ -363,8 +363,10 @@ skv_status launch_fwd(const skv_problem& pb, const void* q, const void* k, const
     SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     const dim3 grid((unsigned)((Qn + BM - 1) / BM), (unsigned)pb.n_heads, (unsigned)pb.P);
     const float scale_log2 = pb.scale * 1.4426950408889634f;
+    skv_host::timer_begin(skv_host::kTimeFwd, c.stream);
     kern<<<grid, kFwdThreads, smem, c.stream>>>(mq, mk, mv, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.m, scale_log2,
                                                 csr, o_part, lse_part, c.status, c.wait_limit);
+    skv_host::timer_end(skv_host::kTimeFwd, c.stream);
     SKV_LAUNCHED();
     return SKV_OK;
 }

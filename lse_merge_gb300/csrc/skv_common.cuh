@@ -63,6 +63,12 @@ skv_status get_ctx(void* stream, Ctx& ctx);
 // Counts one kernel launch of this library (skv_launch_count).
 void note_launch(int n = 1);
 
+// Optional per-kernel CUDA-event timing (skv_set_kernel_timing): slots of the
+// main kernels; begin/end record events on the launching stream when enabled.
+enum TimerSlot { kTimeFwd = 0, kTimeMerge = 1, kTimeBwdKV = 2, kTimeBwdQ = 3, kTimeSlots = 4 };
+void timer_begin(int slot, cudaStream_t stream);
+void timer_end(int slot, cudaStream_t stream);
+
 // Workspace layout helpers (byte offsets, 256-byte aligned).
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 

@@ -204,9 +204,12 @@ namespace skv_internal {
 skv_status launch_merge(const float* o_part, const float* lse_part, int P, int64_t rows, int d, void* o,
                         skv_dtype o_dtype, float* lse, const skv_host::Ctx& c) {
     if (rows == 0) return SKV_OK;
-    if (o_dtype == SKV_BF16)
-        return merge_dispatch(o_part, lse_part, P, rows, d, static_cast<__nv_bfloat16*>(o), lse, c);
-    return merge_dispatch(o_part, lse_part, P, rows, d, static_cast<float*>(o), lse, c);
+    skv_host::timer_begin(skv_host::kTimeMerge, c.stream);
+    const skv_status st =
+        o_dtype == SKV_BF16 ? merge_dispatch(o_part, lse_part, P, rows, d, static_cast<__nv_bfloat16*>(o), lse, c)
+                            : merge_dispatch(o_part, lse_part, P, rows, d, static_cast<float*>(o), lse, c);
+    skv_host::timer_end(skv_host::kTimeMerge, c.stream);
+    return st;
 }
 
 skv_status launch_bwd_prep(const void* o, const void* dO, const float* lse, skv_dtype dt, int64_t Qn, int64_t Qp,
