@@ -337,19 +337,31 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                     }
                 }
                 const float4* l4 = reinterpret_cast<const float4*>(md.lse2 + col0);
+                if (full) {
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 l = l4[j4];
-                    const float lv[4] = {l.x, l.y, l.z, l.w};
-                    float pv[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int j = 4 * j4 + u;
-                        pv[u] = ((keep >> j) & 1u) ? ex2(fmaf(__uint_as_float(sraw[c][j]), scale_log2, -lv[u]))
-                                                   : 0.f;
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 l = l4[j4];
+                        pk[c][2 * j4] = pack_bf16(ex2(fmaf(__uint_as_float(sraw[c][4 * j4]), scale_log2, -l.x)),
+                                                  ex2(fmaf(__uint_as_float(sraw[c][4 * j4 + 1]), scale_log2, -l.y)));
+                        pk[c][2 * j4 + 1] =
+                            pack_bf16(ex2(fmaf(__uint_as_float(sraw[c][4 * j4 + 2]), scale_log2, -l.z)),
+                                      ex2(fmaf(__uint_as_float(sraw[c][4 * j4 + 3]), scale_log2, -l.w)));
                     }
-                    pk[c][2 * j4] = pack_bf16(pv[0], pv[1]);
-                    pk[c][2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
+                } else {
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 l = l4[j4];
+                        const float lv[4] = {l.x, l.y, l.z, l.w};
+                        float pv[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int j = 4 * j4 + u;
+                            pv[u] = ((keep >> j) & 1u) ? ex2(fmaf(__uint_as_float(sraw[c][j]), scale_log2, -lv[u]))
+                                                       : 0.f;
+                        }
+                        pk[c][2 * j4] = pack_bf16(pv[0], pv[1]);
+                        pk[c][2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
+                    }
                 }
             }
             if (!uniform_wait(&bb.dp_full, t & 1)) { ok = false; break; }
@@ -688,9 +700,14 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
                         keep = (b1 >= 32 ? 0xffffffffu : ((1u << b1) - 1u)) & ~((1u << b0) - 1u);
                     }
                 }
+                if (full) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    pr[c][j] = ((keep >> j) & 1u) ? ex2(fmaf(__uint_as_float(sraw[c][j]), scale_log2, -l2)) : 0.f;
+                    for (int j = 0; j < 32; ++j) pr[c][j] = ex2(fmaf(__uint_as_float(sraw[c][j]), scale_log2, -l2));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        pr[c][j] = ((keep >> j) & 1u) ? ex2(fmaf(__uint_as_float(sraw[c][j]), scale_log2, -l2)) : 0.f;
+                }
             }
             if (!uniform_wait(&bb.dp_full, n & 1)) { ok = false; break; }
             tc_fence_after();

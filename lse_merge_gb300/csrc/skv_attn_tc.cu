@@ -1,22 +1,24 @@
-// Tensor-core anchor attention of libskv for GB300 (sm_103a): tcgen05 MMA with
-// TMEM accumulators, TMA-fed bf16 operands, warp-specialised roles.
+// Tensor-core anchor attention forward of libskv for GB300 (sm_103a): tcgen05
+// MMA with TMEM accumulators, TMA-fed bf16 operands, warp-specialised roles.
 //
 // Forward [Split-KV §4.1 Eq. 3; Alg. 1 line 7 of "Split-KV: Efficient Context
-// Parallelism for Training Diffusion Drafters"]: one thread block computes
-// the partial (o_p, l_p) of one 128-row query tile, one head and one virtual
-// rank p.  The key tiles it visits are the 128-key tiles of rank p's chunks
-// that intersect the union of its rows' windows [s_i, a_i) (§3.1 Fig. 1);
-// every other tile is never loaded.  Tiles inside every row's window are
-// processed unmasked; only boundary tiles get the per-row compare.
+// Parallelism for Training Diffusion Drafters"]: one thread block computes the
+// partials (o_p, l_p) of two consecutive 128-row query tiles, one head and one
+// virtual rank p.  The key tiles it visits are the 128-key tiles of rank p's
+// chunks that intersect the union of its rows' windows [s_i, a_i) (§3.1
+// Fig. 1); every other tile is never loaded.  Tiles inside every row's window
+// are processed unmasked; only boundary tiles get the per-row compare.
 //
-// Roles (192 threads):
-//   warps 0-3  softmax: thread r owns query row r; reads S from TMEM, online
-//              max / exp2 / sum, writes bf16 P back to TMEM, rescales O when
-//              the running max grows by more than 2^8, final o_p, l_p.
-//   warp 4     MMA issuer (one thread): S = Q K^T (SS), O += P V (TS).
-//   warp 5     TMA producer (one thread): Q once, K/V tiles through 2 stages.
-// TMEM (512 columns): S double buffer [0,256), O [256,256+D), P double buffer
-// (64 columns each, bf16 pairs) [384,512).
+// The two query tiles share every K/V tile and alternate on the tensor core,
+// so one tile's exponentials overlap the other tile's MMAs.  Roles (320 threads):
+//   warps 0-3, 4-7  softmax of query tile 0, 1: thread owns one row; reads S
+//                   from TMEM, online max / exp2 / sum, bf16 P back to TMEM (over
+//                   S), rescales O when the running max grows by more than 2^8.
+//   warp 8          MMA issuer (one thread): S_j = Q_j K^T (SS), O_j += P_j V (TS).
+//   warp 9          TMA producer (one thread): Q_0, Q_1 once, K/V through 2 stages.
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
+// Issue order per key tile n: PV_0(n), S_0(n+1), PV_1(n), S_1(n+1); hence when
+// S_j(n) has completed, PV_j(n-1) has too and O_j may be rescaled without a wait.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -31,17 +33,18 @@ using namespace skv_ptx;
 using namespace skv_tcc;
 
 constexpr int kStages = 2;
-constexpr int kFwdThreads = 192;
+constexpr int kFwdThreads = 320;
+constexpr int kMmaWarp = 8, kTmaWarp = 9;
 constexpr long long kTeardownWait = 2000000000LL;   // ns; in-flight copies / MMAs end in microseconds
 
 template <int D>
 struct __align__(1024) FwdSmem {
-    __nv_bfloat16 q[D / 64][BM * 64];
+    __nv_bfloat16 q[2][D / 64][BM * 64];
     __nv_bfloat16 k[kStages][D / 64][BN * 64];
     __nv_bfloat16 v[kStages][D / 64][BN * 64];
     uint64_t q_full;
     uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t s_full[2], p_full[2];
     uint64_t mma_fin;
     uint64_t stuck;             // never completed: target of the forced-timeout test mode
     uint32_t tmem_base;
@@ -58,7 +61,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     extern __shared__ unsigned char smem_raw[];
     FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qt = blockIdx.x, h = blockIdx.y, p = blockIdx.z;
+    const int qt0 = 2 * blockIdx.x, h = blockIdx.y, p = blockIdx.z;
     constexpr int NP = D / 64;                       // 64-column panels per row
     constexpr uint32_t kTileBytes = BN * D * 2;      // one K or V tile (== Q tile)
 
@@ -66,10 +69,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     // completes, so the timeout path runs deterministically
     const bool stuck_test = wait_limit < 0;
     if (stuck_test) wait_limit = -wait_limit;
-    TileBounds tb = tile_bounds(s, a, B, Qn, S, qt);
+    const TileBounds tb0 = tile_bounds(s, a, B, Qn, S, qt0);
+    TileBounds tb1 = tb0;
+    if (int64_t(qt0 + 1) * BM < Qn) tb1 = tile_bounds(s, a, B, Qn, S, qt0 + 1);
+    else tb1.lo = S, tb1.hi = 0, tb1.flo = 0, tb1.fhi = 0;
+    int64_t lo = tb0.lo < tb1.lo ? tb0.lo : tb1.lo;
+    int64_t hi = tb0.hi > tb1.hi ? tb0.hi : tb1.hi;
     // once any block of the launch has timed out the result is void: the
     // remaining blocks skip their work instead of each waiting out a deadline
-    if (*(volatile int*)status == SKV_ERR_TIMEOUT) tb.hi = tb.lo;
+    if (*(volatile int*)status == SKV_ERR_TIMEOUT) hi = lo;
 
     if (tid == 0) {
         mbar_init(&sm.q_full, 1);
@@ -81,14 +89,13 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.s_full[i], 1);
             mbar_init(&sm.p_full[i], 128);
-            mbar_init(&sm.o_done[i], 1);
         }
         mbar_init(&sm.mma_fin, 1);
         mbar_init(&sm.stuck, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&sm.tmem_base, 512);
         tmem_relinquish();
     }
@@ -96,33 +103,35 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
-    const uint32_t tS = tmem, tO = tmem + 256, tP = tmem + 384;
 
     TileIter it;
-    it.init(csr, p, p + 1, m, tb.lo, tb.hi);
+    it.init(csr, p, p + 1, m, lo, hi);
+    auto abort_now = [&]() {
+        atomicExch(&sm.abort_flag, 1);
+        skv::raise_status(status, SKV_ERR_TIMEOUT);
+    };
 
-    if (warp == 5) {
+    if (warp == kTmaWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            prefetch_tensormap(&map_q);
-            prefetch_tensormap(&map_k);
-            prefetch_tensormap(&map_v);
             int n = 0;
             int64_t x0;
             bool any = false;
             while (it.next(x0)) {
                 if (!any) {
-                    mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
-                    for (int c = 0; c < NP; ++c) tma_load_2d(sm.q[c], &map_q, &sm.q_full, h * D + c * 64, qt * BM);
+                    prefetch_tensormap(&map_k);
+                    prefetch_tensormap(&map_v);
+                    mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
+                    for (int j = 0; j < 2; ++j)
+                        for (int c = 0; c < NP; ++c)
+                            tma_load_2d(sm.q[j][c], &map_q, &sm.q_full, h * D + c * 64, (qt0 + j) * BM);
                     any = true;
                 }
                 const int st = n % kStages;
-                if (n >= kStages) {
-                    if (!mbar_wait(&sm.kv_empty[st], ((n - kStages) / kStages) & 1, wait_limit, &sm.abort_flag)) {
-                        atomicExch(&sm.abort_flag, 1);
-                        skv::raise_status(status, SKV_ERR_TIMEOUT);
-                        break;
-                    }
+                if (n >= kStages &&
+                    !mbar_wait(&sm.kv_empty[st], ((n - kStages) / kStages) & 1, wait_limit, &sm.abort_flag)) {
+                    abort_now();
+                    break;
                 }
                 if (*(volatile int*)&sm.abort_flag) break;
                 mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
@@ -141,7 +150,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 mbar_wait(&sm.v_full[st], (last / kStages) & 1, kTeardownWait);
             }
         }
-    } else if (warp == 4) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
@@ -152,55 +161,48 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 TileIter cnt = it;
                 while (cnt.next(x0)) ++T;
             }
-            bool ok = true;
+            bool ok = T > 0;
             bool issued = false;   // any MMA in flight to wait for before TMEM is freed
-            auto fail = [&]() {
-                atomicExch(&sm.abort_flag, 1);
-                skv::raise_status(status, SKV_ERR_TIMEOUT);
-                ok = false;
-            };
-            if (stuck_test && !mbar_wait(&sm.stuck, 0, wait_limit, &sm.abort_flag)) fail();
-            auto issue_s = [&](int n) {
+            if (ok && stuck_test && !mbar_wait(&sm.stuck, 0, wait_limit, &sm.abort_flag)) ok = false;
+            if (ok) ok = mbar_wait(&sm.q_full, 0, wait_limit, &sm.abort_flag);
+            auto issue_s = [&](int j, int n) -> bool {    // S_j = Q_j K_n^T -> TMEM [128 j, 128 j + 128)
                 const int st = n % kStages;
-                if (!mbar_wait(&sm.k_full[st], (n / kStages) & 1, wait_limit, &sm.abort_flag)) { fail(); return; }
+                if (!mbar_wait(&sm.k_full[st], (n / kStages) & 1, wait_limit, &sm.abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t dS = tS + (n & 1) * BN;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk & 3) * 32;
-                    const uint64_t ad = smem_desc(smem_u32(sm.q[kk >> 2]) + off, 16, 1024);
-                    const uint64_t bd = smem_desc(smem_u32(sm.k[st][kk >> 2]) + off, 16, 1024);
-                    mma_ss(dS, ad, bd, idS, kk > 0);
+                    mma_ss(tmem + j * 128, smem_desc(smem_u32(sm.q[j][kk >> 2]) + off, 16, 1024),
+                           smem_desc(smem_u32(sm.k[st][kk >> 2]) + off, 16, 1024), idS, kk > 0);
                 }
+                mma_commit(&sm.s_full[j]);
                 issued = true;
-                mma_commit(&sm.s_full[n & 1]);
+                return true;
             };
-            if (T > 0 && ok) {
-                if (!mbar_wait(&sm.q_full, 0, wait_limit, &sm.abort_flag)) fail();
-                if (ok) issue_s(0);
-                for (int n = 0; n < T && ok; ++n) {
-                    if (*(volatile int*)&sm.abort_flag) { ok = false; break; }
-                    if (n + 1 < T) {
-                        issue_s(n + 1);
-                        if (!ok) break;
-                    }
-                    const int st = n % kStages;
-                    if (!mbar_wait(&sm.p_full[n & 1], (n >> 1) & 1, wait_limit, &sm.abort_flag)) { fail(); break; }
-                    if (!mbar_wait(&sm.v_full[st], (n / kStages) & 1, wait_limit, &sm.abort_flag)) { fail(); break; }
-                    tc_fence_after();
-                    const uint32_t aP = tP + (n & 1) * 64;
+            auto issue_pv = [&](int j, int n) -> bool {   // O_j += P_j V_n (bf16 P_j over S_j)
+                const int st = n % kStages;
+                if (!mbar_wait(&sm.p_full[j], n & 1, wait_limit, &sm.abort_flag)) return false;
+                if (!mbar_wait(&sm.v_full[st], (n / kStages) & 1, wait_limit, &sm.abort_flag)) return false;
+                tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t bd = smem_desc(smem_u32(sm.v[st][0]) + kk * 2048, BN * 128, 1024);
-                        mma_ts(tO, aP + kk * 8, bd, idO, (n > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    issued = true;
-                    mma_commit(&sm.o_done[n & 1]);
-                    mma_commit(&sm.kv_empty[st]);
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t bd = smem_desc(smem_u32(sm.v[st][0]) + kk * 2048, BN * 128, 1024);
+                    mma_ts(tmem + 256 + j * 128, tmem + j * 128 + kk * 8, bd, idO, (n > 0 || kk > 0) ? 1u : 0u);
                 }
+                return true;
+            };
+            if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
+            for (int n = 0; ok && n < T; ++n) {
+                if (*(volatile int*)&sm.abort_flag) { ok = false; break; }
+                // S_j(n+1) overwrites S_j right behind the PV_j(n) that reads P_j from it
+                if (!issue_pv(0, n)) { ok = false; break; }
+                if (n + 1 < T && !issue_s(0, n + 1)) { ok = false; break; }
+                if (!issue_pv(1, n)) { ok = false; break; }
+                mma_commit(&sm.kv_empty[n % kStages]);
+                if (n + 1 < T && !issue_s(1, n + 1)) { ok = false; break; }
             }
+            if (!ok && T > 0) abort_now();
             // all MMAs this thread issued have completed before TMEM is freed
-            // (a commit is only made when there is an MMA to track)
             if (issued) {
                 mma_commit(&sm.mma_fin);
                 if (!mbar_wait(&sm.mma_fin, 0, kTeardownWait)) skv::raise_status(status, SKV_ERR_TIMEOUT);
@@ -211,60 +213,69 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         // tcgen05.ld/st are warp-collective: every branch around them is made
         // warp-uniform (__any_sync / __all_sync); per-row choices are data.
         constexpr unsigned kAll = 0xffffffffu;
-        const int r = tid;                         // row inside the tile == TMEM lane
-        const int64_t row = int64_t(qt) * BM + r;
+        const int j = warp >> 2;                       // query tile of this warpgroup
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;                // row inside the tile == TMEM lane
+        const int64_t row = int64_t(qt0 + j) * BM + r;
         const bool live = row < Qn;
+        const TileBounds tb = j ? tb1 : tb0;
         int64_t rlo = 0, rhi = 0;
         if (live) skv::block_window(s, a, (int)(row / B), S, rlo, rhi);
-        const uint32_t lane_base = uint32_t(warp * 32) << 16;
+        const uint32_t lane_base = uint32_t(quad * 32) << 16;
+        const uint32_t tS = tmem + j * 128, tO = tmem + 256 + j * 128;
         float m_ref = -INFINITY, l = 0.f;
-        int o_waited = 0;
         bool ok = true;
         auto uniform_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
             const bool got = mbar_wait_warp(bar, parity, wait_limit, &sm.abort_flag);
-            if (!got && lane == 0) {
-                atomicExch(&sm.abort_flag, 1);
-                skv::raise_status(status, SKV_ERR_TIMEOUT);
-            }
+            if (!got && lane == 0) abort_now();
             return got;
-        };
-        auto wait_o = [&](int need) {
-            while (ok && o_waited < need) {
-                if (!uniform_wait(&sm.o_done[o_waited & 1], (o_waited >> 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                ++o_waited;
-            }
         };
         int64_t x0;
         int n = 0;
         while (ok && it.next(x0)) {
             if (__any_sync(kAll, *(volatile int*)&sm.abort_flag != 0)) { ok = false; break; }
-            if (!uniform_wait(&sm.s_full[n & 1], (n >> 1) & 1)) { ok = false; break; }
+            if (!uniform_wait(&sm.s_full[j], n & 1)) { ok = false; break; }
             tc_fence_after();
-            float sc[BN];
-            {
-                uint32_t raw[BN / 32][32];               // all chunks in flight before one wait
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + (n & 1) * BN + lane_base + c * 32, raw[c]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) sc[c * 32 + j] = __uint_as_float(raw[c][j]);
-            }
+            // pass 1: row max over the tile (two 32-column chunks per TMEM wait)
             const bool full = (x0 >= tb.flo) && (x0 + BN <= tb.fhi);
-            if (!full) {
+            uint32_t keep[BN / 32];
 #pragma unroll
-                for (int j = 0; j < BN; ++j) {
-                    const int64_t x = x0 + j;
-                    if (x < rlo || x >= rhi) sc[j] = -INFINITY;
+            for (int c = 0; c < BN / 32; ++c) {
+                keep[c] = 0xffffffffu;
+                if (!full) {                              // boundary tile: this row's window
+                    const int64_t lo_c = rlo - (x0 + 32 * c), hi_c = rhi - (x0 + 32 * c);
+                    keep[c] = 0u;
+                    if (hi_c > 0 && lo_c < 32) {
+                        const int b0 = lo_c > 0 ? (int)lo_c : 0, b1 = hi_c < 32 ? (int)hi_c : 32;
+                        keep[c] = (b1 >= 32 ? 0xffffffffu : ((1u << b1) - 1u)) & ~((1u << b0) - 1u);
+                    }
                 }
             }
-            float mx = -INFINITY;
+            // independent partial maxima break the 128-long dependency chain
+            float m8[8];
 #pragma unroll
-            for (int j = 0; j < BN; ++j) mx = fmaxf(mx, sc[j]);
+            for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BN / 32; c += 2) {
+                uint32_t raw[2][32];
+                tmem_ld32(tS + lane_base + c * 32, raw[0]);
+                tmem_ld32(tS + lane_base + c * 32 + 32, raw[1]);
+                tmem_ld_wait();
+                if (full) {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) m8[jj & 7] = fmaxf(m8[jj & 7], __uint_as_float(raw[u][jj]));
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj)
+                            if ((keep[c + u] >> jj) & 1u) m8[jj & 7] = fmaxf(m8[jj & 7], __uint_as_float(raw[u][jj]));
+                }
+            }
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             const float mx_s = mx * scale_log2;
             bool rescale = false;
             float alpha = 1.f;
@@ -273,48 +284,67 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 rescale = (l > 0.f);
                 m_ref = mx_s;
             }
-            const bool warp_rescale = __any_sync(kAll, rescale);
-            // P buffer n&1 was last read by PV_{n-2}; O must be final before a rescale
-            wait_o(warp_rescale ? n : n - 1);
-            if (!ok) break;
-            if (warp_rescale) {
+            // O_j is final for tiles < n here: S_j(n) was issued after PV_j(n-1)
+            if (__any_sync(kAll, rescale)) {
                 const float f = rescale ? alpha : 1.f;
-                tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t rr[32];
                     tmem_ld32(tO + lane_base + c * 32, rr);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
+                    for (int jj = 0; jj < 32; ++jj) rr[jj] = __float_as_uint(__uint_as_float(rr[jj]) * f);
                     tmem_st32(tO + lane_base + c * 32, rr);
                 }
             }
             l *= alpha;
-            float sum = 0.f;
+            // pass 2: P = exp2(z scale log2e - m) as bf16 pairs over S_j's first 64 columns;
+            // chunk pair (c, c+1) lands in columns [16c, 16c+32), already read in this pass
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
             const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c) {
+            for (int c = 0; c < BN / 32; c += 2) {
+                uint32_t raw[2][32];
+                tmem_ld32(tS + lane_base + c * 32, raw[0]);
+                tmem_ld32(tS + lane_base + c * 32 + 32, raw[1]);
+                tmem_ld_wait();
                 uint32_t pk[32];
+                if (full) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float z0 = sc[c * 64 + 2 * j], z1 = sc[c * 64 + 2 * j + 1];
-                    const float p0 = (z0 == -INFINITY) ? 0.f : ex2(fmaf(z0, scale_log2, neg));
-                    const float p1 = (z1 == -INFINITY) ? 0.f : ex2(fmaf(z1, scale_log2, neg));
-                    sum += p0 + p1;
-                    pk[j] = pack_bf16(p0, p1);
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const float p0 = ex2(fmaf(__uint_as_float(raw[u][2 * jj]), scale_log2, neg));
+                            const float p1 = ex2(fmaf(__uint_as_float(raw[u][2 * jj + 1]), scale_log2, neg));
+                            s4[jj & 3] += p0 + p1;
+                            pk[u * 16 + jj] = pack_bf16(p0, p1);
+                        }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int e0 = 2 * jj, e1 = 2 * jj + 1;
+                            const float p0 = ((keep[c + u] >> e0) & 1u)
+                                                 ? ex2(fmaf(__uint_as_float(raw[u][e0]), scale_log2, neg)) : 0.f;
+                            const float p1 = ((keep[c + u] >> e1) & 1u)
+                                                 ? ex2(fmaf(__uint_as_float(raw[u][e1]), scale_log2, neg)) : 0.f;
+                            s4[jj & 3] += p0 + p1;
+                            pk[u * 16 + jj] = pack_bf16(p0, p1);
+                        }
                 }
-                tmem_st32(tP + (n & 1) * 64 + lane_base + c * 32, pk);
+                tmem_st32(tS + lane_base + c * 16, pk);
             }
+            const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
             l += sum;
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&sm.p_full[n & 1]);
+            mbar_arrive(&sm.p_full[j]);
             ++n;
         }
-        wait_o(n);
+        // every MMA (the last PV included) has completed once mma_fin fires
         const bool aborted = __any_sync(kAll, *(volatile int*)&sm.abort_flag != 0);
-        if (ok && !aborted) {
+        if (ok && !aborted && (n == 0 || uniform_wait(&sm.mma_fin, 0))) {
             const bool mine = live && l > 0.f;
             const float inv = mine ? 1.f / l : 0.f;
             float* dst = o_part + ((int64_t(p) * Qn + row) * H + h) * D;
@@ -327,11 +357,11 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     tmem_ld_wait();
                     if (mine) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            float4 v4 = make_float4(__uint_as_float(rr[j]) * inv, __uint_as_float(rr[j + 1]) * inv,
-                                                    __uint_as_float(rr[j + 2]) * inv,
-                                                    __uint_as_float(rr[j + 3]) * inv);
-                            __stcs(reinterpret_cast<float4*>(dst + c * 32 + j), v4);
+                        for (int jj = 0; jj < 32; jj += 4) {
+                            float4 v4 = make_float4(__uint_as_float(rr[jj]) * inv, __uint_as_float(rr[jj + 1]) * inv,
+                                                    __uint_as_float(rr[jj + 2]) * inv,
+                                                    __uint_as_float(rr[jj + 3]) * inv);
+                            __stcs(reinterpret_cast<float4*>(dst + c * 32 + jj), v4);
                         }
                     }
                 }
@@ -343,7 +373,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -361,7 +391,8 @@ skv_status launch_fwd(const skv_problem& pb, const void* q, const void* k, const
     if (smem < 120 * 1024) smem = 120 * 1024;   // one block per SM: it owns all 512 TMEM columns
     auto kern = attn_fwd_tc_kernel<D>;
     SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    const dim3 grid((unsigned)((Qn + BM - 1) / BM), (unsigned)pb.n_heads, (unsigned)pb.P);
+    const int64_t n_qt = (Qn + BM - 1) / BM;
+    const dim3 grid((unsigned)((n_qt + 1) / 2), (unsigned)pb.n_heads, (unsigned)pb.P);
     const float scale_log2 = pb.scale * 1.4426950408889634f;
     skv_host::timer_begin(skv_host::kTimeFwd, c.stream);
     kern<<<grid, kFwdThreads, smem, c.stream>>>(mq, mk, mv, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.m, scale_log2,
