@@ -837,7 +837,7 @@ namespace skv_tc {
 
 bool bwd_supported(const skv_problem& pb) {
     return pb.dtype == SKV_BF16 && (pb.head_dim == 64 || pb.head_dim == 128) && pb.m % BN == 0 &&
-           pb.n_heads <= 65535;
+           pb.n_heads <= 65535 && pb.S <= INT32_MAX;
 }
 
 size_t bwd_scratch_bytes(const skv_problem& pb) {

@@ -17,6 +17,7 @@
 //   warp 8          MMA issuer (one thread): S_j = Q_j K^T (SS), O_j += P_j V (TS).
 //   warp 9          TMA producer (one thread): Q_0, Q_1 once, K/V through 2 stages.
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
+// bf16 P_j lies over S_j: keys [0,64) in columns [0,32), keys [64,128) in [64,96).
 // Issue order per key tile n: PV_0(n), S_0(n+1), PV_1(n), S_1(n+1); hence when
 // S_j(n) has completed, PV_j(n-1) has too and O_j may be rescaled without a wait.
 #include <cuda.h>
@@ -167,7 +168,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             if (ok) ok = mbar_wait(&sm.q_full, 0, wait_limit, &sm.abort_flag);
             auto issue_s = [&](int j, int n) -> bool {    // S_j = Q_j K_n^T -> TMEM [128 j, 128 j + 128)
                 const int st = n % kStages;
-                if (!mbar_wait(&sm.k_full[st], (n / kStages) & 1, wait_limit, &sm.abort_flag)) return false;
+                // K_n has landed once S_0(n) could be issued
+                if (j == 0 && !mbar_wait(&sm.k_full[st], (n / kStages) & 1, wait_limit, &sm.abort_flag)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -187,13 +189,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     const uint64_t bd = smem_desc(smem_u32(sm.v[st][0]) + kk * 2048, BN * 128, 1024);
-                    mma_ts(tmem + 256 + j * 128, tmem + j * 128 + kk * 8, bd, idO, (n > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + 256 + j * 128, tmem + j * 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), bd, idO, (n > 0 || kk > 0) ? 1u : 0u);
                 }
                 return true;
             };
             if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
             for (int n = 0; ok && n < T; ++n) {
-                if (*(volatile int*)&sm.abort_flag) { ok = false; break; }
                 // S_j(n+1) overwrites S_j right behind the PV_j(n) that reads P_j from it
                 if (!issue_pv(0, n)) { ok = false; break; }
                 if (n + 1 < T && !issue_s(0, n + 1)) { ok = false; break; }
@@ -218,9 +219,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         const int r = quad * 32 + lane;                // row inside the tile == TMEM lane
         const int64_t row = int64_t(qt0 + j) * BM + r;
         const bool live = row < Qn;
-        const TileBounds tb = j ? tb1 : tb0;
-        int64_t rlo = 0, rhi = 0;
-        if (live) skv::block_window(s, a, (int)(row / B), S, rlo, rhi);
+        // positions fit in int32 here (anchors are int32 and S < 2^31 on this path)
+        int rlo = 0, rhi = 0;
+        {
+            int64_t l64 = 0, h64 = 0;
+            if (live) skv::block_window(s, a, (int)(row / B), S, l64, h64);
+            rlo = (int)l64;
+            rhi = (int)h64;
+        }
+        const int flo = (int)(j ? tb1.flo : tb0.flo), fhi = (int)(j ? tb1.fhi : tb0.fhi);
         const uint32_t lane_base = uint32_t(quad * 32) << 16;
         const uint32_t tS = tmem + j * 128, tO = tmem + 256 + j * 128;
         float m_ref = -INFINITY, l = 0.f;
@@ -236,46 +243,44 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             if (__any_sync(kAll, *(volatile int*)&sm.abort_flag != 0)) { ok = false; break; }
             if (!uniform_wait(&sm.s_full[j], n & 1)) { ok = false; break; }
             tc_fence_after();
-            // pass 1: row max over the tile (two 32-column chunks per TMEM wait)
-            const bool full = (x0 >= tb.flo) && (x0 + BN <= tb.fhi);
-            uint32_t keep[BN / 32];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                keep[c] = 0xffffffffu;
-                if (!full) {                              // boundary tile: this row's window
-                    const int64_t lo_c = rlo - (x0 + 32 * c), hi_c = rhi - (x0 + 32 * c);
-                    keep[c] = 0u;
-                    if (hi_c > 0 && lo_c < 32) {
-                        const int b0 = lo_c > 0 ? (int)lo_c : 0, b1 = hi_c < 32 ? (int)hi_c : 32;
-                        keep[c] = (b1 >= 32 ? 0xffffffffu : ((1u << b1) - 1u)) & ~((1u << b0) - 1u);
-                    }
-                }
-            }
-            // independent partial maxima break the 128-long dependency chain
-            float m8[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < BN / 32; c += 2) {
-                uint32_t raw[2][32];
-                tmem_ld32(tS + lane_base + c * 32, raw[0]);
-                tmem_ld32(tS + lane_base + c * 32 + 32, raw[1]);
+            // scores of chunk pair (cb, cb+1) into registers, -inf outside this row's
+            // window on boundary tiles
+            const int xt = (int)x0;
+            const bool full = (xt >= flo) && (xt + BN <= fhi);
+            auto load_pair = [&](uint32_t (&v)[2][32], int cb) {
+                tmem_ld32(tS + lane_base + cb * 32, v[0]);
+                tmem_ld32(tS + lane_base + cb * 32 + 32, v[1]);
                 tmem_ld_wait();
-                if (full) {
+                if (!full) {
 #pragma unroll
-                    for (int u = 0; u < 2; ++u)
-#pragma unroll
-                        for (int jj = 0; jj < 32; ++jj) m8[jj & 7] = fmaxf(m8[jj & 7], __uint_as_float(raw[u][jj]));
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 2; ++u)
+                    for (int u = 0; u < 2; ++u) {
+                        const int lo_c = rlo - (xt + 32 * (cb + u)), hi_c = rhi - (xt + 32 * (cb + u));
+                        uint32_t keep = 0u;
+                        if (hi_c > 0 && lo_c < 32) {
+                            const int b0 = lo_c > 0 ? lo_c : 0, b1 = hi_c < 32 ? hi_c : 32;
+                            keep = (b1 >= 32 ? 0xffffffffu : ((1u << b1) - 1u)) & ~((1u << b0) - 1u);
+                        }
 #pragma unroll
                         for (int jj = 0; jj < 32; ++jj)
-                            if ((keep[c + u] >> jj) & 1u) m8[jj & 7] = fmaxf(m8[jj & 7], __uint_as_float(raw[u][jj]));
+                            if (!((keep >> jj) & 1u)) v[u][jj] = 0xff800000u;   // -inf
+                    }
                 }
-            }
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            };
+            auto pair_max = [&](const uint32_t (&v)[2][32], float m) {
+                float m2[2] = {m, -INFINITY};
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj += 2)
+                        m2[u] = fmax3(m2[u], __uint_as_float(v[u][jj]), __uint_as_float(v[u][jj + 1]));
+                return fmaxf(m2[0], m2[1]);
+            };
+            // row max over columns [0, 64), then [64, 128) which stay in registers
+            uint32_t sv[2][32];
+            load_pair(sv, 0);
+            float mx = pair_max(sv, -INFINITY);
+            load_pair(sv, 2);
+            mx = pair_max(sv, mx);
             const float mx_s = mx * scale_log2;
             bool rescale = false;
             float alpha = 1.f;
@@ -298,45 +303,30 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 }
             }
             l *= alpha;
-            // pass 2: P = exp2(z scale log2e - m) as bf16 pairs over S_j's first 64 columns;
-            // chunk pair (c, c+1) lands in columns [16c, 16c+32), already read in this pass
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            // P = 2^(z scale log2e - m) as bf16 pairs: keys [64, 128) (in registers) to
+            // TMEM columns [64, 96), then keys [0, 64), re-read, to [0, 32)
             const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            const float2 sc2 = make_float2(scale_log2, scale_log2), ng2 = make_float2(neg, neg);
+            float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            auto pair_exp = [&](const uint32_t (&v)[2][32], uint32_t col) {
 #pragma unroll
-            for (int c = 0; c < BN / 32; c += 2) {
-                uint32_t raw[2][32];
-                tmem_ld32(tS + lane_base + c * 32, raw[0]);
-                tmem_ld32(tS + lane_base + c * 32 + 32, raw[1]);
-                tmem_ld_wait();
-                uint32_t pk[32];
-                if (full) {
+                for (int u = 0; u < 2; ++u) {
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u)
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const float p0 = ex2(fmaf(__uint_as_float(raw[u][2 * jj]), scale_log2, neg));
-                            const float p1 = ex2(fmaf(__uint_as_float(raw[u][2 * jj + 1]), scale_log2, neg));
-                            s4[jj & 3] += p0 + p1;
-                            pk[u * 16 + jj] = pack_bf16(p0, p1);
-                        }
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 2; ++u)
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const int e0 = 2 * jj, e1 = 2 * jj + 1;
-                            const float p0 = ((keep[c + u] >> e0) & 1u)
-                                                 ? ex2(fmaf(__uint_as_float(raw[u][e0]), scale_log2, neg)) : 0.f;
-                            const float p1 = ((keep[c + u] >> e1) & 1u)
-                                                 ? ex2(fmaf(__uint_as_float(raw[u][e1]), scale_log2, neg)) : 0.f;
-                            s4[jj & 3] += p0 + p1;
-                            pk[u * 16 + jj] = pack_bf16(p0, p1);
-                        }
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const float2 z = __ffma2_rn(
+                            make_float2(__uint_as_float(v[u][2 * jj]), __uint_as_float(v[u][2 * jj + 1])), sc2, ng2);
+                        const float2 pv = make_float2(ex2(z.x), ex2(z.y));
+                        sum2[jj & 1] = __fadd2_rn(sum2[jj & 1], pv);
+                        pk[jj] = pack_bf16(pv.x, pv.y);
+                    }
+                    tmem_st16(tS + lane_base + col + u * 16, pk);
                 }
-                tmem_st32(tS + lane_base + c * 16, pk);
-            }
-            const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-            l += sum;
+            };
+            pair_exp(sv, 64);
+            load_pair(sv, 0);
+            pair_exp(sv, 0);
+            l += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&sm.p_full[j]);
@@ -408,7 +398,7 @@ namespace skv_tc {
 
 bool fwd_supported(const skv_problem& pb) {
     return pb.dtype == SKV_BF16 && (pb.head_dim == 64 || pb.head_dim == 128) && pb.m % BN == 0 &&
-           pb.P <= 65535 && pb.n_heads <= 65535;
+           pb.P <= 65535 && pb.n_heads <= 65535 && pb.S <= INT32_MAX;
 }
 size_t fwd_scratch_bytes(const skv_problem&) { return 0; }
 

@@ -235,6 +235,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// three-input maximum (sm_100+), one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31) == 0; }
 
 }  // namespace skv_ptx
