@@ -166,6 +166,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             bool issued = false;   // any MMA in flight to wait for before TMEM is freed
             if (ok && stuck_test && !mbar_wait(&sm.stuck, 0, wait_limit, &sm.abort_flag)) ok = false;
             if (ok) ok = mbar_wait(&sm.q_full, 0, wait_limit, &sm.abort_flag);
+            // shared-memory descriptors: the start-address field (bytes / 16) of a panel,
+            // stage or K step is an offset from the first one (every address < 256 KiB)
+            constexpr uint32_t kPanel = BN * 64 * 2 / 16, kStage = NP * kPanel;
+            const uint64_t dq = smem_desc(smem_u32(sm.q[0][0]), 16, 1024);
+            const uint64_t dk = smem_desc(smem_u32(sm.k[0][0]), 16, 1024);
+            const uint64_t dv = smem_desc(smem_u32(sm.v[0][0]), BN * 128, 1024);
             auto issue_s = [&](int j, int n) -> bool {    // S_j = Q_j K_n^T -> TMEM [128 j, 128 j + 128)
                 const int st = n % kStages;
                 // K_n has landed once S_0(n) could be issued
@@ -173,9 +179,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    mma_ss(tmem + j * 128, smem_desc(smem_u32(sm.q[j][kk >> 2]) + off, 16, 1024),
-                           smem_desc(smem_u32(sm.k[st][kk >> 2]) + off, 16, 1024), idS, kk > 0);
+                    const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+                    mma_ss(tmem + j * 128, dq + (j * kStage + off), dk + (st * kStage + off), idS, kk > 0);
                 }
                 mma_commit(&sm.s_full[j]);
                 issued = true;
@@ -184,13 +189,13 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             auto issue_pv = [&](int j, int n) -> bool {   // O_j += P_j V_n (bf16 P_j over S_j)
                 const int st = n % kStages;
                 if (!mbar_wait(&sm.p_full[j], n & 1, wait_limit, &sm.abort_flag)) return false;
-                if (!mbar_wait(&sm.v_full[st], (n / kStages) & 1, wait_limit, &sm.abort_flag)) return false;
+                // V_n has landed once PV_0(n) could be issued
+                if (j == 0 && !mbar_wait(&sm.v_full[st], (n / kStages) & 1, wait_limit, &sm.abort_flag)) return false;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t bd = smem_desc(smem_u32(sm.v[st][0]) + kk * 2048, BN * 128, 1024);
-                    mma_ts(tmem + 256 + j * 128, tmem + j * 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), bd, idO, (n > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tmem + 256 + j * 128, tmem + j * 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                           dv + (st * kStage + kk * 128), idO, (n > 0 || kk > 0) ? 1u : 0u);
                 return true;
             };
             if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
