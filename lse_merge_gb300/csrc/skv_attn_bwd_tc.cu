@@ -20,7 +20,8 @@
 //    every rank's chunks that meet the tile's windows: dq = sum_p dq^(p)
 //    (Alg. 1 line 17) is accumulated in TMEM and written once.  Per key tile:
 //      S = Q K^T, dP = dO V^T (SS); eight warps form dS (bf16 -> TMEM over S);
-//      dQ += dS K (TS).
+//      dQ += dS K (TS).  dP of the next tile is issued as soon as dP has been
+//      read, ahead of the dQ MMA, so it overlaps the forming of dS.
 // Recomputing S and dP in the second kernel costs two extra GEMMs per tile pair
 // but removes every dq reduction from the key-stationary loop.
 #include <cuda.h>
@@ -102,7 +103,7 @@ struct KvMeta {                                      // per query tile, loaded w
 };
 
 struct KvBars {
-    uint64_t kv_full, qd_full[2], qd_empty[2], s_full, s_read, dp_full, ds_full, mma_fin;
+    uint64_t kv_full, q_full[2], q_empty[2], do_full[2], do_empty[2], s_full, s_read, dp_full, ds_full, mma_fin;
     uint64_t stuck;                                  // never completed: target of the forced-timeout test mode
     uint32_t tmem_base;
     int abort_flag;
@@ -151,8 +152,10 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
     if (tid == 0) {
         mbar_init(&bb.kv_full, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bb.qd_full[i], 1);
-            mbar_init(&bb.qd_empty[i], 1);
+            mbar_init(&bb.q_full[i], 1);
+            mbar_init(&bb.q_empty[i], 1);
+            mbar_init(&bb.do_full[i], 1);
+            mbar_init(&bb.do_empty[i], 1);
         }
         mbar_init(&bb.s_full, 1);
         mbar_init(&bb.s_read, 256);
@@ -187,10 +190,12 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 tma_load_2d(tl.k[c], &map_k, &bb.kv_full, h * D + c * 64, (int)x0);
                 tma_load_2d(tl.v[c], &map_v, &bb.kv_full, h * D + c * 64, (int)x0);
             }
-            int t = 0;
-            for (; t < cnt; ++t) {
+            // Q (with the tile's metadata) and dO have their own rings: the dK MMA frees
+            // Q before the dV MMA frees dO, and S of a tile needs Q before dP needs dO
+            int nq = 0, nd = 0;
+            for (int t = 0; t < cnt; ++t) {
                 const int st = t & 1;
-                if (t >= 2 && !mbar_wait(&bb.qd_empty[st], ((t - 2) >> 1) & 1, wait_limit, &bb.abort_flag)) {
+                if (t >= 2 && !mbar_wait(&bb.q_empty[st], ((t - 2) >> 1) & 1, wait_limit, &bb.abort_flag)) {
                     abort_now();
                     break;
                 }
@@ -199,19 +204,35 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 const int row = qt * BM;
                 sm.meta[st].qt = qt;                     // made visible by the arrive below
                 sm.meta[st].bnd = qtb[qt];
-                mbar_arrive_expect_tx(&bb.qd_full[st], 2 * kTile + 2 * BM * 4);
-                for (int c = 0; c < NP; ++c) {
-                    tma_load_2d(tl.q[st][c], &map_q, &bb.qd_full[st], h * D + c * 64, row);
-                    tma_load_2d(tl.dO[st][c], &map_do, &bb.qd_full[st], h * D + c * 64, row);
+                mbar_arrive_expect_tx(&bb.q_full[st], kTile + 2 * BM * 4);
+                for (int c = 0; c < NP; ++c) tma_load_2d(tl.q[st][c], &map_q, &bb.q_full[st], h * D + c * 64, row);
+                bulk_load(sm.meta[st].lse2, lse2_hm + int64_t(h) * Qp + row, BM * 4, &bb.q_full[st]);
+                bulk_load(sm.meta[st].D, D_hm + int64_t(h) * Qp + row, BM * 4, &bb.q_full[st]);
+                ++nq;
+                if (t >= 2 && !mbar_wait(&bb.do_empty[st], ((t - 2) >> 1) & 1, wait_limit, &bb.abort_flag)) {
+                    abort_now();
+                    break;
                 }
-                bulk_load(sm.meta[st].lse2, lse2_hm + int64_t(h) * Qp + row, BM * 4, &bb.qd_full[st]);
-                bulk_load(sm.meta[st].D, D_hm + int64_t(h) * Qp + row, BM * 4, &bb.qd_full[st]);
+                mbar_arrive_expect_tx(&bb.do_full[st], kTile);
+                for (int c = 0; c < NP; ++c) tma_load_2d(tl.dO[st][c], &map_do, &bb.do_full[st], h * D + c * 64, row);
+                ++nd;
+                // the tile loaded after the next one: into L2 now, so that its load,
+                // issued once this stage is released, does not wait on HBM
+                if (t + 2 < cnt) {
+                    const int row2 = list[t + 2] * BM;
+                    for (int c = 0; c < NP; ++c) {
+                        tma_prefetch_2d(&map_q, h * D + c * 64, row2);
+                        tma_prefetch_2d(&map_do, h * D + c * 64, row2);
+                    }
+                    bulk_prefetch_l2(lse2_hm + int64_t(h) * Qp + row2, BM * 4);
+                    bulk_prefetch_l2(D_hm + int64_t(h) * Qp + row2, BM * 4);
+                }
             }
             // every copy issued has landed before the block exits
             mbar_wait(&bb.kv_full, 0, kTeardownWait);
-            for (int st = 0; st < 2 && st < t; ++st) {
-                const int last = st + ((t - 1 - st) >> 1) * 2;
-                mbar_wait(&bb.qd_full[st], (last >> 1) & 1, kTeardownWait);
+            for (int st = 0; st < 2; ++st) {
+                if (st < nq) mbar_wait(&bb.q_full[st], (((nq - 1 - st) >> 1) * 2 + st) >> 1 & 1, kTeardownWait);
+                if (st < nd) mbar_wait(&bb.do_full[st], (((nd - 1 - st) >> 1) * 2 + st) >> 1 & 1, kTeardownWait);
             }
         }
     } else if (warp == kKvMma) {
@@ -222,41 +243,50 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             bool issued = false;
             bool ok = !(stuck_test && !mbar_wait(&bb.stuck, 0, wait_limit, &bb.abort_flag));
             if (ok) ok = mbar_wait(&bb.kv_full, 0, wait_limit, &bb.abort_flag);
+            // shared-memory descriptors as offsets (bytes / 16) from the first panel
+            constexpr uint32_t kPanel = BN * 64 * 2 / 16, kSt = NP * kPanel;
+            const uint64_t dK = smem_desc(smem_u32(tl.k[0]), 16, 1024), dV = smem_desc(smem_u32(tl.v[0]), 16, 1024);
+            const uint64_t dQ = smem_desc(smem_u32(tl.q[0][0]), 16, 1024);
+            const uint64_t dDO = smem_desc(smem_u32(tl.dO[0][0]), 16, 1024);
+            const uint64_t dQmn = smem_desc(smem_u32(tl.q[0][0]), BM * 128, 1024);
+            const uint64_t dDOmn = smem_desc(smem_u32(tl.dO[0][0]), BM * 128, 1024);
             auto issue_s = [&](int st) {                   // S^T = K Q^T -> A
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    mma_ss(tA, smem_desc(smem_u32(tl.k[kk >> 2]) + off, 16, 1024),
-                           smem_desc(smem_u32(tl.q[st][kk >> 2]) + off, 16, 1024), idS, kk > 0);
+                    const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+                    mma_ss(tA, dK + off, dQ + (st * kSt + off), idS, kk > 0);
                 }
                 mma_commit(&bb.s_full);
             };
             auto issue_dp = [&](int st) {                  // dP^T = V dO^T -> B
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    mma_ss(tB, smem_desc(smem_u32(tl.v[kk >> 2]) + off, 16, 1024),
-                           smem_desc(smem_u32(tl.dO[st][kk >> 2]) + off, 16, 1024), idS, kk > 0);
+                    const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+                    mma_ss(tB, dV + off, dDO + (st * kSt + off), idS, kk > 0);
                 }
                 mma_commit(&bb.dp_full);
             };
-            if (ok) ok = mbar_wait(&bb.qd_full[0], 0, wait_limit, &bb.abort_flag);
+            if (ok) ok = mbar_wait(&bb.q_full[0], 0, wait_limit, &bb.abort_flag);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
-                issue_dp(0);
                 issued = true;
+                ok = mbar_wait(&bb.do_full[0], 0, wait_limit, &bb.abort_flag);
+            }
+            if (ok) {
+                tc_fence_after();
+                issue_dp(0);
             }
             // per query tile t:
             //   [S_t read]  S_{t+1} -> A   (overlaps the compute warps' P_t / dS_t)
-            //   [dS_t done] dV_t += P_t dO_t, dK_t += dS_t Q_t (P_t, dS_t bf16 in B over the
+            //   [dS_t done] dK_t += dS_t Q_t, dV_t += P_t dO_t (P_t, dS_t bf16 in B over the
             //               read dP_t), then dP_{t+1} -> B behind them in issue order
             for (int t = 0; ok && t < cnt; ++t) {
                 const int st = t & 1;
                 const bool more = t + 1 < cnt;
                 if (!mbar_wait(&bb.s_read, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
                 if (more) {
-                    if (!mbar_wait(&bb.qd_full[(t + 1) & 1], ((t + 1) >> 1) & 1, wait_limit, &bb.abort_flag)) {
+                    if (!mbar_wait(&bb.q_full[(t + 1) & 1], ((t + 1) >> 1) & 1, wait_limit, &bb.abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -265,21 +295,28 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 }
                 if (!mbar_wait(&bb.ds_full, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                // dV += P^T dO.  bf16 P^T of query columns [64h, 64h+64) sits in TMEM
-                // columns [64h, 64h+32) of B (each half of the compute warps writes inside its half)
+                // dK += dS^T Q.  bf16 P^T of query columns [64h, 64h+64) sits in TMEM columns
+                // [64h, 64h+32) of B and dS^T in [64h+32, 64h+64) (each half of the compute
+                // warps writes inside its half)
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts(tdV, tB + (kk >> 2) * 64 + (kk & 3) * 8,
-                           smem_desc(smem_u32(tl.dO[st][0]) + kk * 2048, BM * 128, 1024), idKV,
+                    mma_ts(tdK, tB + (kk >> 2) * 64 + 32 + (kk & 3) * 8, dQmn + (st * kSt + kk * 128), idKV,
                            (t > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bb.q_empty[st]);
 #pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)      // dK += dS^T Q (bf16 dS^T in B, after P^T)
-                    mma_ts(tdK, tB + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
-                           smem_desc(smem_u32(tl.q[st][0]) + kk * 2048, BM * 128, 1024), idKV,
+                for (int kk = 0; kk < BM / 16; ++kk)      // dV += P^T dO
+                    mma_ts(tdV, tB + (kk >> 2) * 64 + (kk & 3) * 8, dDOmn + (st * kSt + kk * 128), idKV,
                            (t > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bb.qd_empty[st]);
-                // dP_{t+1} overwrites B right behind the dV and dK MMAs reading P_t, dS_t from it
-                if (more) issue_dp((t + 1) & 1);
+                mma_commit(&bb.do_empty[st]);
+                // dP_{t+1} overwrites B right behind the dK and dV MMAs reading dS_t, P_t from it
+                if (more) {
+                    if (!mbar_wait(&bb.do_full[(t + 1) & 1], ((t + 1) >> 1) & 1, wait_limit, &bb.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_dp((t + 1) & 1);
+                }
             }
             if (!ok) abort_now();
             if (issued) {
@@ -305,7 +342,7 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
         for (int t = 0; t < cnt; ++t) {
             const int st = t & 1;
             if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
-            if (!uniform_wait(&bb.qd_full[st], (t >> 1) & 1)) { ok = false; break; }
+            if (!uniform_wait(&bb.q_full[st], (t >> 1) & 1)) { ok = false; break; }
             const KvMeta& md = sm.meta[st];
             const int64_t row0 = int64_t(md.qt) * BM;
             const int4 bnd = md.bnd;
@@ -338,14 +375,18 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 }
                 const float4* l4 = reinterpret_cast<const float4*>(md.lse2 + col0);
                 if (full) {
+                    const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
                         const float4 l = l4[j4];
-                        pk[c][2 * j4] = pack_bf16(ex2(fmaf(__uint_as_float(sraw[c][4 * j4]), scale_log2, -l.x)),
-                                                  ex2(fmaf(__uint_as_float(sraw[c][4 * j4 + 1]), scale_log2, -l.y)));
-                        pk[c][2 * j4 + 1] =
-                            pack_bf16(ex2(fmaf(__uint_as_float(sraw[c][4 * j4 + 2]), scale_log2, -l.z)),
-                                      ex2(fmaf(__uint_as_float(sraw[c][4 * j4 + 3]), scale_log2, -l.w)));
+                        const float2 z0 = __ffma2_rn(make_float2(__uint_as_float(sraw[c][4 * j4]),
+                                                                 __uint_as_float(sraw[c][4 * j4 + 1])),
+                                                     sc2, make_float2(-l.x, -l.y));
+                        const float2 z1 = __ffma2_rn(make_float2(__uint_as_float(sraw[c][4 * j4 + 2]),
+                                                                 __uint_as_float(sraw[c][4 * j4 + 3])),
+                                                     sc2, make_float2(-l.z, -l.w));
+                        pk[c][2 * j4] = pack_bf16(ex2(z0.x), ex2(z0.y));
+                        pk[c][2 * j4 + 1] = pack_bf16(ex2(z1.x), ex2(z1.y));
                     }
                 } else {
 #pragma unroll
@@ -382,12 +423,16 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const float4 dd = d4[j4];
-                    const float2 p01 = unpack_bf16(pk[c][2 * j4]);
-                    const float2 p23 = unpack_bf16(pk[c][2 * j4 + 1]);
-                    d2[c][2 * j4] = pack_bf16(p01.x * (__uint_as_float(draw[c][4 * j4]) - dd.x),
-                                              p01.y * (__uint_as_float(draw[c][4 * j4 + 1]) - dd.y));
-                    d2[c][2 * j4 + 1] = pack_bf16(p23.x * (__uint_as_float(draw[c][4 * j4 + 2]) - dd.z),
-                                                  p23.y * (__uint_as_float(draw[c][4 * j4 + 3]) - dd.w));
+                    const float2 t01 = __fadd2_rn(
+                        make_float2(__uint_as_float(draw[c][4 * j4]), __uint_as_float(draw[c][4 * j4 + 1])),
+                        make_float2(-dd.x, -dd.y));
+                    const float2 t23 = __fadd2_rn(
+                        make_float2(__uint_as_float(draw[c][4 * j4 + 2]), __uint_as_float(draw[c][4 * j4 + 3])),
+                        make_float2(-dd.z, -dd.w));
+                    const float2 d01 = __fmul2_rn(unpack_bf16(pk[c][2 * j4]), t01);
+                    const float2 d23 = __fmul2_rn(unpack_bf16(pk[c][2 * j4 + 1]), t23);
+                    d2[c][2 * j4] = pack_bf16(d01.x, d01.y);
+                    d2[c][2 * j4 + 1] = pack_bf16(d23.x, d23.y);
                 }
             }
             // bf16 dS^T of columns [64hf + 32c, +32) -> TMEM B columns [64hf + 32 + 16c, +16)
@@ -459,7 +504,7 @@ struct QMeta {
 
 struct QBars {
     uint64_t q_full, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-    uint64_t s_full[2], dp_full, ds_full, mma_fin, stuck;
+    uint64_t s_full[2], dp_full, dp_read, ds_full, mma_fin, stuck;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -513,6 +558,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
         mbar_init(&bb.s_full[0], 1);
         mbar_init(&bb.s_full[1], 1);
         mbar_init(&bb.dp_full, 1);
+        mbar_init(&bb.dp_read, 256);
         mbar_init(&bb.ds_full, 256);
         mbar_init(&bb.mma_fin, 1);
         mbar_init(&bb.stuck, 1);
@@ -538,8 +584,11 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
         if (lane == 0) {
             int n = 0;       // key tiles whose K load was issued
             int nv = 0;      // key tiles whose V load was issued
-            int64_t x0;
+            int64_t x0, xa;
             bool any = false;
+            // K/V of the tile two ahead go to L2 while this one loads
+            TileIter ahead = it;
+            for (int i = 0; i < 2; ++i) ahead.next(xa);
             while (it.next(x0)) {
                 if (!any) {
                     prefetch_tensormap(&map_k);
@@ -563,6 +612,11 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
                 mbar_arrive_expect_tx(&bb.k_full[ks], kTile);
                 for (int c = 0; c < NP; ++c) tma_load_2d(tl.k[ks][c], &map_k, &bb.k_full[ks], h * D + c * 64, (int)x0);
                 ++n;
+                if (ahead.next(xa))
+                    for (int c = 0; c < NP; ++c) {
+                        tma_prefetch_2d(&map_k, h * D + c * 64, (int)xa);
+                        tma_prefetch_2d(&map_v, h * D + c * 64, (int)xa);
+                    }
                 if (n - 1 >= kVStages &&
                     !mbar_wait(&bb.v_empty[vs], ((n - 1 - kVStages) / kVStages) & 1, wait_limit, &bb.abort_flag)) {
                     abort_now();
@@ -598,15 +652,19 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
             bool ok = T > 0;
             if (ok && stuck_test && !mbar_wait(&bb.stuck, 0, wait_limit, &bb.abort_flag)) ok = false;
             if (ok) ok = mbar_wait(&bb.q_full, 0, wait_limit, &bb.abort_flag);
+            // shared-memory descriptors as offsets (bytes / 16) from the first panel
+            constexpr uint32_t kPanel = BN * 64 * 2 / 16, kSt = NP * kPanel;
+            const uint64_t dQ = smem_desc(smem_u32(tl.q[0]), 16, 1024), dDO = smem_desc(smem_u32(tl.dO[0]), 16, 1024);
+            const uint64_t dK = smem_desc(smem_u32(tl.k[0][0]), 16, 1024), dV = smem_desc(smem_u32(tl.v[0][0]), 16, 1024);
+            const uint64_t dKmn = smem_desc(smem_u32(tl.k[0][0]), BN * 128, 1024);
             auto issue_s = [&](int n) -> bool {            // S_n = Q K_n^T -> S[n&1]
                 const int ks = n % kKStages;
                 if (!mbar_wait(&bb.k_full[ks], (n / kKStages) & 1, wait_limit, &bb.abort_flag)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    mma_ss(tS + (n & 1) * 128, smem_desc(smem_u32(tl.q[kk >> 2]) + off, 16, 1024),
-                           smem_desc(smem_u32(tl.k[ks][kk >> 2]) + off, 16, 1024), idS, kk > 0);
+                    const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+                    mma_ss(tS + (n & 1) * 128, dQ + off, dK + (ks * kSt + off), idS, kk > 0);
                 }
                 mma_commit(&bb.s_full[n & 1]);
                 issued = true;
@@ -618,9 +676,8 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    mma_ss(tP, smem_desc(smem_u32(tl.dO[kk >> 2]) + off, 16, 1024),
-                           smem_desc(smem_u32(tl.v[vs][kk >> 2]) + off, 16, 1024), idS, kk > 0);
+                    const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+                    mma_ss(tP, dDO + off, dV + (vs * kSt + off), idS, kk > 0);
                 }
                 mma_commit(&bb.dp_full);
                 mma_commit(&bb.v_empty[vs]);
@@ -629,6 +686,13 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
             };
             if (ok) ok = issue_s(0) && issue_dp(0) && (T < 2 || issue_s(1));
             for (int n = 0; ok && n < T; ++n) {
+                // dP_{n+1} overwrites dP as soon as the compute warps have read dP_n,
+                // ahead of the dQ MMA that waits for dS_n
+                if (n + 1 < T) {
+                    if (!mbar_wait(&bb.dp_read, n & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    if (!issue_dp(n + 1)) { ok = false; break; }
+                }
                 if (!mbar_wait(&bb.ds_full, n & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 // dQ += dS_n K_n: bf16 dS of key columns [64h, 64h+64) sits in TMEM columns
@@ -636,12 +700,9 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
                 const int ks = n % kKStages;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tQ, tS + (n & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
-                           smem_desc(smem_u32(tl.k[ks][0]) + kk * 2048, BN * 128, 1024), idQ,
+                    mma_ts(tQ, tS + (n & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8, dKmn + (ks * kSt + kk * 128), idQ,
                            (n > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bb.k_empty[ks]);
-                // dP held dP_n, which the compute warps finished reading before ds_full
-                if (n + 1 < T && !issue_dp(n + 1)) { ok = false; break; }
                 // S_{n+2} overwrites S[n&1] right behind the dQ MMA that reads dS_n from it
                 if (n + 2 < T && !issue_s(n + 2)) { ok = false; break; }
             }
@@ -701,8 +762,14 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
                     }
                 }
                 if (full) {
+                    const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-l2, -l2);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) pr[c][j] = ex2(fmaf(__uint_as_float(sraw[c][j]), scale_log2, -l2));
+                    for (int j = 0; j < 32; j += 2) {
+                        const float2 z = __ffma2_rn(
+                            make_float2(__uint_as_float(sraw[c][j]), __uint_as_float(sraw[c][j + 1])), sc2, nl2);
+                        pr[c][j] = ex2(z.x);
+                        pr[c][j + 1] = ex2(z.y);
+                    }
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
@@ -715,13 +782,19 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
             tmem_ld32(tP + lane_base + hf * 64, draw[0]);
             tmem_ld32(tP + lane_base + hf * 64 + 32, draw[1]);
             tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&bb.dp_read);                    // dP is free for the next tile
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t pk[16];
+                const float2 nd2 = make_float2(-Dr, -Dr);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    pk[j] = pack_bf16(pr[c][2 * j] * (__uint_as_float(draw[c][2 * j]) - Dr),
-                                      pr[c][2 * j + 1] * (__uint_as_float(draw[c][2 * j + 1]) - Dr));
+                for (int j = 0; j < 16; ++j) {
+                    const float2 t = __fadd2_rn(
+                        make_float2(__uint_as_float(draw[c][2 * j]), __uint_as_float(draw[c][2 * j + 1])), nd2);
+                    const float2 d = __fmul2_rn(make_float2(pr[c][2 * j], pr[c][2 * j + 1]), t);
+                    pk[j] = pack_bf16(d.x, d.y);
+                }
                 // bf16 dS of key columns [64hf + 32c, +32) -> TMEM columns [64hf + 16c, +16)
                 // of this S buffer: inside this warp's half, over columns read already
                 tmem_st16(sbuf + lane_base + hf * 64 + c * 16, pk);
