@@ -153,66 +153,77 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
-            constexpr uint32_t idO = idesc_bf16_f32(BM, D, 0, 1);
-            int64_t x0;
-            int T = 0;
-            {
-                TileIter cnt = it;
-                while (cnt.next(x0)) ++T;
-            }
-            bool ok = T > 0;
-            bool issued = false;   // any MMA in flight to wait for before TMEM is freed
-            if (ok && stuck_test && !mbar_wait(&sm.stuck, 0, wait_limit, &sm.abort_flag)) ok = false;
-            if (ok) ok = mbar_wait(&sm.q_full, 0, wait_limit, &sm.abort_flag);
-            // shared-memory descriptors: the start-address field (bytes / 16) of a panel,
-            // stage or K step is an offset from the first one (every address < 256 KiB)
-            constexpr uint32_t kPanel = BN * 64 * 2 / 16, kStage = NP * kPanel;
-            const uint64_t dq = smem_desc(smem_u32(sm.q[0][0]), 16, 1024);
-            const uint64_t dk = smem_desc(smem_u32(sm.k[0][0]), 16, 1024);
-            const uint64_t dv = smem_desc(smem_u32(sm.v[0][0]), BN * 128, 1024);
-            auto issue_s = [&](int j, int n) -> bool {    // S_j = Q_j K_n^T -> TMEM [128 j, 128 j + 128)
-                const int st = n % kStages;
-                // K_n has landed once S_0(n) could be issued
-                if (j == 0 && !mbar_wait(&sm.k_full[st], (n / kStages) & 1, wait_limit, &sm.abort_flag)) return false;
-                tc_fence_after();
+        // The whole warp runs the schedule, so descriptors and counters are
+        // warp-uniform; one elected lane issues each group of MMAs and its commit.
+        constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
+        constexpr uint32_t idO = idesc_bf16_f32(BM, D, 0, 1);
+        int64_t x0;
+        int T = 0;
+        {
+            TileIter cnt = it;
+            while (cnt.next(x0)) ++T;
+        }
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            return mbar_wait_warp(bar, parity, wait_limit, &sm.abort_flag);
+        };
+        bool ok = T > 0;
+        bool issued = false;   // any MMA in flight to wait for before TMEM is freed
+        if (ok && stuck_test && !wait(&sm.stuck, 0)) ok = false;
+        if (ok) ok = wait(&sm.q_full, 0);
+        // shared-memory descriptors: the start-address field (bytes / 16) of a panel,
+        // stage or K step is an offset from the first one (every address < 256 KiB)
+        constexpr uint32_t kPanel = BN * 64 * 2 / 16, kStage = NP * kPanel;
+        const uint64_t dq = smem_desc(smem_u32(sm.q[0][0]), 16, 1024);
+        const uint64_t dk = smem_desc(smem_u32(sm.k[0][0]), 16, 1024);
+        const uint64_t dv = smem_desc(smem_u32(sm.v[0][0]), BN * 128, 1024);
+        auto issue_s = [&](int j, int n) -> bool {    // S_j = Q_j K_n^T -> TMEM [128 j, 128 j + 128)
+            const int st = n % kStages;
+            // K_n has landed once S_0(n) could be issued
+            if (j == 0 && !wait(&sm.k_full[st], (n / kStages) & 1)) return false;
+            tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
                     mma_ss(tmem + j * 128, dq + (j * kStage + off), dk + (st * kStage + off), idS, kk > 0);
                 }
                 mma_commit(&sm.s_full[j]);
-                issued = true;
-                return true;
-            };
-            auto issue_pv = [&](int j, int n) -> bool {   // O_j += P_j V_n (bf16 P_j over S_j)
-                const int st = n % kStages;
-                if (!mbar_wait(&sm.p_full[j], n & 1, wait_limit, &sm.abort_flag)) return false;
-                // V_n has landed once PV_0(n) could be issued
-                if (j == 0 && !mbar_wait(&sm.v_full[st], (n / kStages) & 1, wait_limit, &sm.abort_flag)) return false;
-                tc_fence_after();
+            }
+            __syncwarp();
+            issued = true;
+            return true;
+        };
+        auto issue_pv = [&](int j, int n) -> bool {   // O_j += P_j V_n (bf16 P_j over S_j)
+            const int st = n % kStages;
+            if (!wait(&sm.p_full[j], n & 1)) return false;
+            // V_n has landed once PV_0(n) could be issued
+            if (j == 0 && !wait(&sm.v_full[st], (n / kStages) & 1)) return false;
+            tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_ts(tmem + 256 + j * 128, tmem + j * 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
                            dv + (st * kStage + kk * 128), idO, (n > 0 || kk > 0) ? 1u : 0u);
-                return true;
-            };
-            if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
-            for (int n = 0; ok && n < T; ++n) {
-                // S_j(n+1) overwrites S_j right behind the PV_j(n) that reads P_j from it
-                if (!issue_pv(0, n)) { ok = false; break; }
-                if (n + 1 < T && !issue_s(0, n + 1)) { ok = false; break; }
-                if (!issue_pv(1, n)) { ok = false; break; }
-                mma_commit(&sm.kv_empty[n % kStages]);
-                if (n + 1 < T && !issue_s(1, n + 1)) { ok = false; break; }
+                if (j == 1) mma_commit(&sm.kv_empty[st]);   // both PVs of tile n have read V_n
             }
-            if (!ok && T > 0) abort_now();
-            // all MMAs this thread issued have completed before TMEM is freed
-            if (issued) {
-                mma_commit(&sm.mma_fin);
-                if (!mbar_wait(&sm.mma_fin, 0, kTeardownWait)) skv::raise_status(status, SKV_ERR_TIMEOUT);
-            }
+            __syncwarp();
+            return true;
+        };
+        if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
+        for (int n = 0; ok && n < T; ++n) {
+            // S_j(n+1) overwrites S_j right behind the PV_j(n) that reads P_j from it
+            if (!issue_pv(0, n)) { ok = false; break; }
+            if (n + 1 < T && !issue_s(0, n + 1)) { ok = false; break; }
+            if (!issue_pv(1, n)) { ok = false; break; }
+            if (n + 1 < T && !issue_s(1, n + 1)) { ok = false; break; }
+        }
+        if (!ok && T > 0 && lane == 0) abort_now();
+        // all MMAs the warp issued have completed before TMEM is freed
+        if (issued) {
+            if (elect_one()) mma_commit(&sm.mma_fin);
+            __syncwarp();
+            if (!mbar_wait_warp(&sm.mma_fin, 0, kTeardownWait) && lane == 0)
+                skv::raise_status(status, SKV_ERR_TIMEOUT);
         }
     } else {
         // ------------------------------------------------------------ softmax

@@ -255,6 +255,17 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return y;
 }
 
-__device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31) == 0; }
+// One lane of a converged warp (the lowest active one) is elected: the MMA
+// issuers run their schedule on the whole warp, so descriptors and counters are
+// warp-uniform, and only the elected lane issues tcgen05.mma / commit.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
 
 }  // namespace skv_ptx
