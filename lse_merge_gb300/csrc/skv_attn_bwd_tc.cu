@@ -237,12 +237,17 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
         }
     } else if (warp == kKvMma) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && cnt > 0) {
+        // the whole warp runs the schedule (warp-uniform descriptors and counters);
+        // one elected lane issues each group of MMAs and its commits
+        if (cnt > 0) {
             constexpr uint32_t idS = idesc_bf16_f32(BN, BM, 0, 0);    // M = keys, N = queries, K = d
             constexpr uint32_t idKV = idesc_bf16_f32(BN, D, 0, 1);    // M = keys, N = d, K = queries
+            auto wait = [&](uint64_t* bar, uint32_t parity) {
+                return mbar_wait_warp(bar, parity, wait_limit, &bb.abort_flag);
+            };
             bool issued = false;
-            bool ok = !(stuck_test && !mbar_wait(&bb.stuck, 0, wait_limit, &bb.abort_flag));
-            if (ok) ok = mbar_wait(&bb.kv_full, 0, wait_limit, &bb.abort_flag);
+            bool ok = !(stuck_test && !wait(&bb.stuck, 0));
+            if (ok) ok = wait(&bb.kv_full, 0);
             // shared-memory descriptors as offsets (bytes / 16) from the first panel
             constexpr uint32_t kPanel = BN * 64 * 2 / 16, kSt = NP * kPanel;
             const uint64_t dK = smem_desc(smem_u32(tl.k[0]), 16, 1024), dV = smem_desc(smem_u32(tl.v[0]), 16, 1024);
@@ -251,27 +256,33 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             const uint64_t dQmn = smem_desc(smem_u32(tl.q[0][0]), BM * 128, 1024);
             const uint64_t dDOmn = smem_desc(smem_u32(tl.dO[0][0]), BM * 128, 1024);
             auto issue_s = [&](int st) {                   // S^T = K Q^T -> A
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
-                    mma_ss(tA, dK + off, dQ + (st * kSt + off), idS, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+                        mma_ss(tA, dK + off, dQ + (st * kSt + off), idS, kk > 0);
+                    }
+                    mma_commit(&bb.s_full);
                 }
-                mma_commit(&bb.s_full);
+                __syncwarp();
             };
             auto issue_dp = [&](int st) {                  // dP^T = V dO^T -> B
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
-                    mma_ss(tB, dV + off, dDO + (st * kSt + off), idS, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+                        mma_ss(tB, dV + off, dDO + (st * kSt + off), idS, kk > 0);
+                    }
+                    mma_commit(&bb.dp_full);
                 }
-                mma_commit(&bb.dp_full);
+                __syncwarp();
             };
-            if (ok) ok = mbar_wait(&bb.q_full[0], 0, wait_limit, &bb.abort_flag);
+            if (ok) ok = wait(&bb.q_full[0], 0);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
                 issued = true;
-                ok = mbar_wait(&bb.do_full[0], 0, wait_limit, &bb.abort_flag);
+                ok = wait(&bb.do_full[0], 0);
             }
             if (ok) {
                 tc_fence_after();
@@ -284,44 +295,43 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             for (int t = 0; ok && t < cnt; ++t) {
                 const int st = t & 1;
                 const bool more = t + 1 < cnt;
-                if (!mbar_wait(&bb.s_read, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
+                if (!wait(&bb.s_read, t & 1)) { ok = false; break; }
                 if (more) {
-                    if (!mbar_wait(&bb.q_full[(t + 1) & 1], ((t + 1) >> 1) & 1, wait_limit, &bb.abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!wait(&bb.q_full[(t + 1) & 1], ((t + 1) >> 1) & 1)) { ok = false; break; }
                     tc_fence_after();
                     issue_s((t + 1) & 1);
                 }
-                if (!mbar_wait(&bb.ds_full, t & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
+                if (!wait(&bb.ds_full, t & 1)) { ok = false; break; }
                 tc_fence_after();
                 // dK += dS^T Q.  bf16 P^T of query columns [64h, 64h+64) sits in TMEM columns
                 // [64h, 64h+32) of B and dS^T in [64h+32, 64h+64) (each half of the compute
                 // warps writes inside its half)
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_ts(tdK, tB + (kk >> 2) * 64 + 32 + (kk & 3) * 8, dQmn + (st * kSt + kk * 128), idKV,
-                           (t > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bb.q_empty[st]);
+                    for (int kk = 0; kk < BM / 16; ++kk)
+                        mma_ts(tdK, tB + (kk >> 2) * 64 + 32 + (kk & 3) * 8, dQmn + (st * kSt + kk * 128), idKV,
+                               (t > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bb.q_empty[st]);
 #pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)      // dV += P^T dO
-                    mma_ts(tdV, tB + (kk >> 2) * 64 + (kk & 3) * 8, dDOmn + (st * kSt + kk * 128), idKV,
-                           (t > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bb.do_empty[st]);
+                    for (int kk = 0; kk < BM / 16; ++kk)  // dV += P^T dO
+                        mma_ts(tdV, tB + (kk >> 2) * 64 + (kk & 3) * 8, dDOmn + (st * kSt + kk * 128), idKV,
+                               (t > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bb.do_empty[st]);
+                }
+                __syncwarp();
                 // dP_{t+1} overwrites B right behind the dK and dV MMAs reading dS_t, P_t from it
                 if (more) {
-                    if (!mbar_wait(&bb.do_full[(t + 1) & 1], ((t + 1) >> 1) & 1, wait_limit, &bb.abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!wait(&bb.do_full[(t + 1) & 1], ((t + 1) >> 1) & 1)) { ok = false; break; }
                     tc_fence_after();
                     issue_dp((t + 1) & 1);
                 }
             }
-            if (!ok) abort_now();
+            if (!ok && lane == 0) abort_now();
             if (issued) {
-                mma_commit(&bb.mma_fin);
-                if (!mbar_wait(&bb.mma_fin, 0, kTeardownWait)) skv::raise_status(status, SKV_ERR_TIMEOUT);
+                if (elect_one()) mma_commit(&bb.mma_fin);
+                __syncwarp();
+                if (!mbar_wait_warp(&bb.mma_fin, 0, kTeardownWait) && lane == 0)
+                    skv::raise_status(status, SKV_ERR_TIMEOUT);
             }
         }
     } else {
@@ -639,41 +649,49 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
         }
     } else if (warp == kQMma) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);    // M = queries, N = keys, K = d
-            constexpr uint32_t idQ = idesc_bf16_f32(BM, D, 0, 1);     // M = queries, N = d, K = keys
-            int T = 0;
-            {
-                TileIter cnt = it;
-                int64_t x0;
-                while (cnt.next(x0)) ++T;
-            }
-            bool issued = false;
-            bool ok = T > 0;
-            if (ok && stuck_test && !mbar_wait(&bb.stuck, 0, wait_limit, &bb.abort_flag)) ok = false;
-            if (ok) ok = mbar_wait(&bb.q_full, 0, wait_limit, &bb.abort_flag);
-            // shared-memory descriptors as offsets (bytes / 16) from the first panel
-            constexpr uint32_t kPanel = BN * 64 * 2 / 16, kSt = NP * kPanel;
-            const uint64_t dQ = smem_desc(smem_u32(tl.q[0]), 16, 1024), dDO = smem_desc(smem_u32(tl.dO[0]), 16, 1024);
-            const uint64_t dK = smem_desc(smem_u32(tl.k[0][0]), 16, 1024), dV = smem_desc(smem_u32(tl.v[0][0]), 16, 1024);
-            const uint64_t dKmn = smem_desc(smem_u32(tl.k[0][0]), BN * 128, 1024);
-            auto issue_s = [&](int n) -> bool {            // S_n = Q K_n^T -> S[n&1]
-                const int ks = n % kKStages;
-                if (!mbar_wait(&bb.k_full[ks], (n / kKStages) & 1, wait_limit, &bb.abort_flag)) return false;
-                tc_fence_after();
+        // the whole warp runs the schedule (warp-uniform descriptors and counters);
+        // one elected lane issues each group of MMAs and its commits
+        constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);    // M = queries, N = keys, K = d
+        constexpr uint32_t idQ = idesc_bf16_f32(BM, D, 0, 1);     // M = queries, N = d, K = keys
+        int T = 0;
+        {
+            TileIter cnt = it;
+            int64_t x0;
+            while (cnt.next(x0)) ++T;
+        }
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            return mbar_wait_warp(bar, parity, wait_limit, &bb.abort_flag);
+        };
+        bool issued = false;
+        bool ok = T > 0;
+        if (ok && stuck_test && !wait(&bb.stuck, 0)) ok = false;
+        if (ok) ok = wait(&bb.q_full, 0);
+        // shared-memory descriptors as offsets (bytes / 16) from the first panel
+        constexpr uint32_t kPanel = BN * 64 * 2 / 16, kSt = NP * kPanel;
+        const uint64_t dQ = smem_desc(smem_u32(tl.q[0]), 16, 1024), dDO = smem_desc(smem_u32(tl.dO[0]), 16, 1024);
+        const uint64_t dK = smem_desc(smem_u32(tl.k[0][0]), 16, 1024), dV = smem_desc(smem_u32(tl.v[0][0]), 16, 1024);
+        const uint64_t dKmn = smem_desc(smem_u32(tl.k[0][0]), BN * 128, 1024);
+        auto issue_s = [&](int n) -> bool {            // S_n = Q K_n^T -> S[n&1]
+            const int ks = n % kKStages;
+            if (!wait(&bb.k_full[ks], (n / kKStages) & 1)) return false;
+            tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
                     mma_ss(tS + (n & 1) * 128, dQ + off, dK + (ks * kSt + off), idS, kk > 0);
                 }
                 mma_commit(&bb.s_full[n & 1]);
-                issued = true;
-                return true;
-            };
-            auto issue_dp = [&](int n) -> bool {           // dP_n = dO V_n^T -> dP
-                const int vs = n % kVStages;
-                if (!mbar_wait(&bb.v_full[vs], (n / kVStages) & 1, wait_limit, &bb.abort_flag)) return false;
-                tc_fence_after();
+            }
+            __syncwarp();
+            issued = true;
+            return true;
+        };
+        auto issue_dp = [&](int n) -> bool {           // dP_n = dO V_n^T -> dP
+            const int vs = n % kVStages;
+            if (!wait(&bb.v_full[vs], (n / kVStages) & 1)) return false;
+            tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
@@ -681,36 +699,42 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
                 }
                 mma_commit(&bb.dp_full);
                 mma_commit(&bb.v_empty[vs]);
-                issued = true;
-                return true;
-            };
-            if (ok) ok = issue_s(0) && issue_dp(0) && (T < 2 || issue_s(1));
-            for (int n = 0; ok && n < T; ++n) {
-                // dP_{n+1} overwrites dP as soon as the compute warps have read dP_n,
-                // ahead of the dQ MMA that waits for dS_n
-                if (n + 1 < T) {
-                    if (!mbar_wait(&bb.dp_read, n & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    if (!issue_dp(n + 1)) { ok = false; break; }
-                }
-                if (!mbar_wait(&bb.ds_full, n & 1, wait_limit, &bb.abort_flag)) { ok = false; break; }
+            }
+            __syncwarp();
+            issued = true;
+            return true;
+        };
+        if (ok) ok = issue_s(0) && issue_dp(0) && (T < 2 || issue_s(1));
+        for (int n = 0; ok && n < T; ++n) {
+            // dP_{n+1} overwrites dP as soon as the compute warps have read dP_n,
+            // ahead of the dQ MMA that waits for dS_n
+            if (n + 1 < T) {
+                if (!wait(&bb.dp_read, n & 1)) { ok = false; break; }
                 tc_fence_after();
-                // dQ += dS_n K_n: bf16 dS of key columns [64h, 64h+64) sits in TMEM columns
-                // [64h, 64h+32) of S[n&1]
-                const int ks = n % kKStages;
+                if (!issue_dp(n + 1)) { ok = false; break; }
+            }
+            if (!wait(&bb.ds_full, n & 1)) { ok = false; break; }
+            tc_fence_after();
+            // dQ += dS_n K_n: bf16 dS of key columns [64h, 64h+64) sits in TMEM columns
+            // [64h, 64h+32) of S[n&1]
+            const int ks = n % kKStages;
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tQ, tS + (n & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8, dKmn + (ks * kSt + kk * 128), idQ,
-                           (n > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tQ, tS + (n & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8, dKmn + (ks * kSt + kk * 128),
+                           idQ, (n > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bb.k_empty[ks]);
-                // S_{n+2} overwrites S[n&1] right behind the dQ MMA that reads dS_n from it
-                if (n + 2 < T && !issue_s(n + 2)) { ok = false; break; }
             }
-            if (!ok && T > 0) abort_now();
-            if (issued) {
-                mma_commit(&bb.mma_fin);
-                if (!mbar_wait(&bb.mma_fin, 0, kTeardownWait)) skv::raise_status(status, SKV_ERR_TIMEOUT);
-            }
+            __syncwarp();
+            // S_{n+2} overwrites S[n&1] right behind the dQ MMA that reads dS_n from it
+            if (n + 2 < T && !issue_s(n + 2)) { ok = false; break; }
+        }
+        if (!ok && T > 0 && lane == 0) abort_now();
+        if (issued) {
+            if (elect_one()) mma_commit(&bb.mma_fin);
+            __syncwarp();
+            if (!mbar_wait_warp(&bb.mma_fin, 0, kTeardownWait) && lane == 0)
+                skv::raise_status(status, SKV_ERR_TIMEOUT);
         }
     } else {
         // ------------------------------------------------------------ compute warps 0-7
