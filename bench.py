@@ -46,6 +46,19 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def csrc_digest():
+    """sha256 over the CUDA library's sources: DRAM-traffic figures captured
+    with ncu are reported only while the kernels are the ones captured."""
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "lse_merge_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -324,8 +337,11 @@ def run_ours(args):
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
     if dom and os.path.exists(tr_path):
         with open(tr_path) as f:
-            per_pair = json.load(f).get(dom, {}).get("dram_bytes_per_useful_pair_head")
-        traffic = per_pair * pairs if per_pair else None
+            tr = json.load(f)
+        per_pair = tr.get(dom, {}).get("dram_bytes_per_useful_pair_head")
+        # null once the kernels differ from the ones the counters were taken on
+        if per_pair and tr.get("csrc_sha256") == csrc_digest():
+            traffic = per_pair * pairs
 
     # end to end through the public API with host buffers (pinned), copies inside
     e2e = None
