@@ -653,12 +653,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
         // one elected lane issues each group of MMAs and its commits
         constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);    // M = queries, N = keys, K = d
         constexpr uint32_t idQ = idesc_bf16_f32(BM, D, 0, 1);     // M = queries, N = d, K = keys
-        int T = 0;
-        {
-            TileIter cnt = it;
-            int64_t x0;
-            while (cnt.next(x0)) ++T;
-        }
+        const int T = it.count();
         auto wait = [&](uint64_t* bar, uint32_t parity) {
             return mbar_wait_warp(bar, parity, wait_limit, &bb.abort_flag);
         };
@@ -931,6 +926,15 @@ skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const
 }  // namespace
 
 namespace skv_tc {
+
+skv_status launch_qtile_bounds(const skv_problem& pb, int4* out, const skv_host::Ctx& c) {
+    const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
+    const int64_t n_qt = (Qn + BM - 1) / BM;
+    if (n_qt == 0) return SKV_OK;
+    qtile_bounds_kernel<<<(unsigned)((n_qt + 127) / 128), 128, 0, c.stream>>>(pb.s, pb.a, pb.B, Qn, pb.S, (int)n_qt, out);
+    SKV_LAUNCHED();
+    return SKV_OK;
+}
 
 bool bwd_supported(const skv_problem& pb) {
     return pb.dtype == SKV_BF16 && (pb.head_dim == 64 || pb.head_dim == 128) && pb.m % BN == 0 &&

@@ -37,6 +37,7 @@ constexpr int kStages = 2;
 constexpr int kFwdThreads = 320;
 constexpr int kMmaWarp = 8, kTmaWarp = 9;
 constexpr long long kTeardownWait = 2000000000LL;   // ns; in-flight copies / MMAs end in microseconds
+constexpr int kListCap = 64;                          // chunk indices staged in shared memory
 
 template <int D>
 struct __align__(1024) FwdSmem {
@@ -48,6 +49,8 @@ struct __align__(1024) FwdSmem {
     uint64_t s_full[2], p_full[2];
     uint64_t mma_fin;
     uint64_t stuck;             // never completed: target of the forced-timeout test mode
+    int32_t clist[kListCap];    // rank p's chunk indices (when they fit)
+    int list_off, list_n;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -57,8 +60,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_v, const int32_t* __restrict__ s,
                    const int32_t* __restrict__ a, int B, int64_t Qn, int H, int64_t S, int m,
-                   float scale_log2, skv::RankCSR csr, float* __restrict__ o_part, float* __restrict__ lse_part,
-                   int* status, long long wait_limit) {
+                   float scale_log2, skv::RankCSR csr, const int4* __restrict__ qtb, int n_qt,
+                   float* __restrict__ o_part, float* __restrict__ lse_part, int* status, long long wait_limit) {
     extern __shared__ unsigned char smem_raw[];
     FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -70,10 +73,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     // completes, so the timeout path runs deterministically
     const bool stuck_test = wait_limit < 0;
     if (stuck_test) wait_limit = -wait_limit;
-    const TileBounds tb0 = tile_bounds(s, a, B, Qn, S, qt0);
-    TileBounds tb1 = tb0;
-    if (int64_t(qt0 + 1) * BM < Qn) tb1 = tile_bounds(s, a, B, Qn, S, qt0 + 1);
-    else tb1.lo = S, tb1.hi = 0, tb1.flo = 0, tb1.fhi = 0;
+    // the tiles' key bounds (union and full-visibility range), computed by a pre-pass
+    const int4 b0 = qtb[qt0];
+    const int4 b1 = qt0 + 1 < n_qt ? qtb[qt0 + 1] : make_int4((int)S, 0, 0, 0);
+    const TileBounds tb0{b0.x, b0.y, b0.z, b0.w}, tb1{b1.x, b1.y, b1.z, b1.w};
     int64_t lo = tb0.lo < tb1.lo ? tb0.lo : tb1.lo;
     int64_t hi = tb0.hi > tb1.hi ? tb0.hi : tb1.hi;
     // once any block of the launch has timed out the result is void: the
@@ -100,13 +103,22 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         tmem_alloc(&sm.tmem_base, 512);
         tmem_relinquish();
     }
+    if (warp == 0) {   // rank p's chunk list into shared memory, one coalesced read
+        const int c0 = csr.ptr[p], nc = csr.ptr[p + 1] - c0;
+        if (nc <= kListCap)
+            for (int i = lane; i < nc; i += 32) sm.clist[i] = csr.list[c0 + i];
+        if (lane == 0) {
+            sm.list_off = c0;
+            sm.list_n = nc;
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
     TileIter it;
-    it.init(csr, p, p + 1, m, lo, hi);
+    it.init_list(sm.list_n <= kListCap ? sm.clist : csr.list + sm.list_off, sm.list_n, m, lo, hi);
     auto abort_now = [&]() {
         atomicExch(&sm.abort_flag, 1);
         skv::raise_status(status, SKV_ERR_TIMEOUT);
@@ -157,12 +169,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         // warp-uniform; one elected lane issues each group of MMAs and its commit.
         constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
         constexpr uint32_t idO = idesc_bf16_f32(BM, D, 0, 1);
-        int64_t x0;
-        int T = 0;
-        {
-            TileIter cnt = it;
-            while (cnt.next(x0)) ++T;
-        }
+        const int T = it.count();
         auto wait = [&](uint64_t* bar, uint32_t parity) {
             return mbar_wait_warp(bar, parity, wait_limit, &sm.abort_flag);
         };
@@ -387,7 +394,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 
 template <int D>
 skv_status launch_fwd(const skv_problem& pb, const void* q, const void* k, const void* v, skv::RankCSR csr,
-                      float* o_part, float* lse_part, const skv_host::Ctx& c) {
+                      float* o_part, float* lse_part, void* scratch, const skv_host::Ctx& c) {
     const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
     CUtensorMap mq, mk, mv;
     if (!make_map(&mq, q, Qn, int64_t(pb.n_heads) * D) || !make_map(&mk, k, pb.S, int64_t(pb.n_heads) * D) ||
@@ -398,11 +405,14 @@ skv_status launch_fwd(const skv_problem& pb, const void* q, const void* k, const
     auto kern = attn_fwd_tc_kernel<D>;
     SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     const int64_t n_qt = (Qn + BM - 1) / BM;
+    int4* qtb = static_cast<int4*>(scratch);
+    skv_status st = skv_tc::launch_qtile_bounds(pb, qtb, c);
+    if (st != SKV_OK) return st;
     const dim3 grid((unsigned)((n_qt + 1) / 2), (unsigned)pb.n_heads, (unsigned)pb.P);
     const float scale_log2 = pb.scale * 1.4426950408889634f;
     skv_host::timer_begin(skv_host::kTimeFwd, c.stream);
     kern<<<grid, kFwdThreads, smem, c.stream>>>(mq, mk, mv, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.m, scale_log2,
-                                                csr, o_part, lse_part, c.status, c.wait_limit);
+                                                csr, qtb, (int)n_qt, o_part, lse_part, c.status, c.wait_limit);
     skv_host::timer_end(skv_host::kTimeFwd, c.stream);
     SKV_LAUNCHED();
     return SKV_OK;
@@ -416,12 +426,15 @@ bool fwd_supported(const skv_problem& pb) {
     return pb.dtype == SKV_BF16 && (pb.head_dim == 64 || pb.head_dim == 128) && pb.m % BN == 0 &&
            pb.P <= 65535 && pb.n_heads <= 65535 && pb.S <= INT32_MAX;
 }
-size_t fwd_scratch_bytes(const skv_problem&) { return 0; }
+size_t fwd_scratch_bytes(const skv_problem& pb) {   // per query tile key bounds (int4)
+    const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
+    return size_t((Qn + BM - 1) / BM) * sizeof(int4);
+}
 
 skv_status launch_attn_fwd_tc(const skv_problem& pb, const void* q, const void* k, const void* v, skv::RankCSR csr,
-                              float* o_part, float* lse_part, void*, const skv_host::Ctx& c) {
-    if (pb.head_dim == 128) return launch_fwd<128>(pb, q, k, v, csr, o_part, lse_part, c);
-    return launch_fwd<64>(pb, q, k, v, csr, o_part, lse_part, c);
+                              float* o_part, float* lse_part, void* scratch, const skv_host::Ctx& c) {
+    if (pb.head_dim == 128) return launch_fwd<128>(pb, q, k, v, csr, o_part, lse_part, scratch, c);
+    return launch_fwd<64>(pb, q, k, v, csr, o_part, lse_part, scratch, c);
 }
 
 }  // namespace skv_tc

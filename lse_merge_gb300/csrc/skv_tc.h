@@ -8,6 +8,8 @@ namespace skv_tc {
 
 bool fwd_supported(const skv_problem& pb);
 bool bwd_supported(const skv_problem& pb);
+// Per 128-row query tile: (union lo, hi, full-visibility lo, hi) of its rows' key windows.
+skv_status launch_qtile_bounds(const skv_problem& pb, int4* out, const skv_host::Ctx& c);
 size_t fwd_scratch_bytes(const skv_problem& pb);
 size_t bwd_scratch_bytes(const skv_problem& pb);
 

@@ -39,22 +39,37 @@ __device__ __forceinline__ TileBounds tile_bounds(const int32_t* s, const int32_
     return tb;
 }
 
-// Walks the 128-key tiles of rank p's chunks that intersect [lo, hi).  Every
-// role runs its own copy and sees the same sequence.
+// Walks the 128-key tiles of a chunk list (rank-major, ascending inside a rank)
+// that intersect [lo, hi).  Every role runs its own copy and sees the same sequence.
 struct TileIter {
     const int32_t* list;
     int ci, ce, m;
     int64_t x, xe, lo, hi;
     // ranks [p0, p1): the CSR list is rank-major, ascending inside a rank
     __device__ __forceinline__ void init(skv::RankCSR csr, int p0, int p1, int m_, int64_t lo_, int64_t hi_) {
-        list = csr.list;
-        ci = csr.ptr[p0];
-        ce = csr.ptr[p1];
+        init_list(csr.list + csr.ptr[p0], csr.ptr[p1] - csr.ptr[p0], m_, lo_, hi_);
+    }
+    // an explicit list of n chunk indices (global or shared memory)
+    __device__ __forceinline__ void init_list(const int32_t* list_, int n, int m_, int64_t lo_, int64_t hi_) {
+        list = list_;
+        ci = 0;
+        ce = n;
         m = m_;
         lo = lo_;
         hi = hi_;
         x = 0;
         xe = 0;
+    }
+    // number of tiles a fresh iterator yields, chunk by chunk (no per-tile stepping)
+    __device__ __forceinline__ int count() const {
+        int T = 0;
+        for (int i = ci; i < ce; ++i) {
+            const int64_t cl = int64_t(list[i]) * m;
+            const int64_t a0 = cl > lo ? cl : lo;
+            const int64_t a1 = (cl + m) < hi ? (cl + m) : hi;
+            if (a0 < a1) T += (int)((a1 - (a0 & ~int64_t(BN - 1)) + BN - 1) / BN);
+        }
+        return T;
     }
     __device__ __forceinline__ bool next(int64_t& x0) {
         while (x >= xe) {
