@@ -14,10 +14,13 @@
 //   warps 0-3, 4-7  softmax of query tile 0, 1: thread owns one row; reads S
 //                   from TMEM, online max / exp2 / sum, bf16 P back to TMEM (over
 //                   S), rescales O when the running max grows by more than 2^8.
-//   warp 8          MMA issuer (one thread): S_j = Q_j K^T (SS), O_j += P_j V (TS).
+//   warp 8          MMA issuer (one elected lane): S_j = Q_j K^T (SS), O_j += P_j V (TS).
 //   warp 9          TMA producer (one thread): Q_0, Q_1 once, K/V through 2 stages.
+//   warps 10-11     none (they complete the third warpgroup, whose registers go to
+//                   the softmax warpgroups).
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
-// bf16 P_j lies over S_j: keys [0,64) in columns [0,32), keys [64,128) in [64,96).
+// bf16 P_j lies over the first 64 columns of S_j (read whole into registers first).
+// The softmax warpgroups take 216 registers per thread, the issuing warpgroup 64.
 // Issue order per key tile n: PV_0(n), S_0(n+1), PV_1(n), S_1(n+1); hence when
 // S_j(n) has completed, PV_j(n-1) has too and O_j may be rescaled without a wait.
 #include <cuda.h>
@@ -34,8 +37,10 @@ using namespace skv_ptx;
 using namespace skv_tcc;
 
 constexpr int kStages = 2;
-constexpr int kFwdThreads = 320;
-constexpr int kMmaWarp = 8, kTmaWarp = 9;
+constexpr int kFwdThreads = 384;                     // warpgroups: softmax 0, softmax 1, MMA/TMA
+constexpr int kMmaWarp = 8, kTmaWarp = 9;            // warps 10-11 only hand their registers over
+constexpr int kRegLaunch = 168, kRegSoftmax = 216, kRegIssue = 64;   // per thread
+static_assert(2 * 128 * kRegSoftmax + 128 * kRegIssue <= kFwdThreads * kRegLaunch, "register split");
 constexpr long long kTeardownWait = 2000000000LL;   // ns; in-flight copies / MMAs end in microseconds
 constexpr int kListCap = 64;                          // chunk indices staged in shared memory
 
@@ -124,115 +129,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         skv::raise_status(status, SKV_ERR_TIMEOUT);
     };
 
-    if (warp == kTmaWarp) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int n = 0;
-            int64_t x0;
-            bool any = false;
-            while (it.next(x0)) {
-                if (!any) {
-                    prefetch_tensormap(&map_k);
-                    prefetch_tensormap(&map_v);
-                    mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
-                    for (int j = 0; j < 2; ++j)
-                        for (int c = 0; c < NP; ++c)
-                            tma_load_2d(sm.q[j][c], &map_q, &sm.q_full, h * D + c * 64, (qt0 + j) * BM);
-                    any = true;
-                }
-                const int st = n % kStages;
-                if (n >= kStages &&
-                    !mbar_wait(&sm.kv_empty[st], ((n - kStages) / kStages) & 1, wait_limit, &sm.abort_flag)) {
-                    abort_now();
-                    break;
-                }
-                if (*(volatile int*)&sm.abort_flag) break;
-                mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
-                for (int c = 0; c < NP; ++c)
-                    tma_load_2d(sm.k[st][c], &map_k, &sm.k_full[st], h * D + c * 64, (int)x0);
-                mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-                for (int c = 0; c < NP; ++c)
-                    tma_load_2d(sm.v[st][c], &map_v, &sm.v_full[st], h * D + c * 64, (int)x0);
-                ++n;
-            }
-            // every load this thread issued has landed before the block exits
-            if (any) mbar_wait(&sm.q_full, 0, kTeardownWait);
-            for (int st = 0; st < kStages && st < n; ++st) {
-                const int last = st + ((n - 1 - st) / kStages) * kStages;   // last tile using stage st
-                mbar_wait(&sm.k_full[st], (last / kStages) & 1, kTeardownWait);
-                mbar_wait(&sm.v_full[st], (last / kStages) & 1, kTeardownWait);
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        // The whole warp runs the schedule, so descriptors and counters are
-        // warp-uniform; one elected lane issues each group of MMAs and its commit.
-        constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
-        constexpr uint32_t idO = idesc_bf16_f32(BM, D, 0, 1);
-        const int T = it.count();
-        auto wait = [&](uint64_t* bar, uint32_t parity) {
-            return mbar_wait_warp(bar, parity, wait_limit, &sm.abort_flag);
-        };
-        bool ok = T > 0;
-        bool issued = false;   // any MMA in flight to wait for before TMEM is freed
-        if (ok && stuck_test && !wait(&sm.stuck, 0)) ok = false;
-        if (ok) ok = wait(&sm.q_full, 0);
-        // shared-memory descriptors: the start-address field (bytes / 16) of a panel,
-        // stage or K step is an offset from the first one (every address < 256 KiB)
-        constexpr uint32_t kPanel = BN * 64 * 2 / 16, kStage = NP * kPanel;
-        const uint64_t dq = smem_desc(smem_u32(sm.q[0][0]), 16, 1024);
-        const uint64_t dk = smem_desc(smem_u32(sm.k[0][0]), 16, 1024);
-        const uint64_t dv = smem_desc(smem_u32(sm.v[0][0]), BN * 128, 1024);
-        auto issue_s = [&](int j, int n) -> bool {    // S_j = Q_j K_n^T -> TMEM [128 j, 128 j + 128)
-            const int st = n % kStages;
-            // K_n has landed once S_0(n) could be issued
-            if (j == 0 && !wait(&sm.k_full[st], (n / kStages) & 1)) return false;
-            tc_fence_after();
-            if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
-                    mma_ss(tmem + j * 128, dq + (j * kStage + off), dk + (st * kStage + off), idS, kk > 0);
-                }
-                mma_commit(&sm.s_full[j]);
-            }
-            __syncwarp();
-            issued = true;
-            return true;
-        };
-        auto issue_pv = [&](int j, int n) -> bool {   // O_j += P_j V_n (bf16 P_j over S_j)
-            const int st = n % kStages;
-            if (!wait(&sm.p_full[j], n & 1)) return false;
-            // V_n has landed once PV_0(n) could be issued
-            if (j == 0 && !wait(&sm.v_full[st], (n / kStages) & 1)) return false;
-            tc_fence_after();
-            if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tmem + 256 + j * 128, tmem + j * 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                           dv + (st * kStage + kk * 128), idO, (n > 0 || kk > 0) ? 1u : 0u);
-                if (j == 1) mma_commit(&sm.kv_empty[st]);   // both PVs of tile n have read V_n
-            }
-            __syncwarp();
-            return true;
-        };
-        if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
-        for (int n = 0; ok && n < T; ++n) {
-            // S_j(n+1) overwrites S_j right behind the PV_j(n) that reads P_j from it
-            if (!issue_pv(0, n)) { ok = false; break; }
-            if (n + 1 < T && !issue_s(0, n + 1)) { ok = false; break; }
-            if (!issue_pv(1, n)) { ok = false; break; }
-            if (n + 1 < T && !issue_s(1, n + 1)) { ok = false; break; }
-        }
-        if (!ok && T > 0 && lane == 0) abort_now();
-        // all MMAs the warp issued have completed before TMEM is freed
-        if (issued) {
-            if (elect_one()) mma_commit(&sm.mma_fin);
-            __syncwarp();
-            if (!mbar_wait_warp(&sm.mma_fin, 0, kTeardownWait) && lane == 0)
-                skv::raise_status(status, SKV_ERR_TIMEOUT);
-        }
-    } else {
+    if (warp < 8) {
+        warpgroup_reg_alloc<kRegSoftmax>();
         // ------------------------------------------------------------ softmax
         // tcgen05.ld/st are warp-collective: every branch around them is made
         // warp-uniform (__any_sync / __all_sync); per-row choices are data.
@@ -266,44 +164,38 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             if (__any_sync(kAll, *(volatile int*)&sm.abort_flag != 0)) { ok = false; break; }
             if (!uniform_wait(&sm.s_full[j], n & 1)) { ok = false; break; }
             tc_fence_after();
-            // scores of chunk pair (cb, cb+1) into registers, -inf outside this row's
-            // window on boundary tiles
+            // the row's 128 scores in registers (one TMEM round), -inf outside this
+            // row's window on boundary tiles
             const int xt = (int)x0;
             const bool full = (xt >= flo) && (xt + BN <= fhi);
-            auto load_pair = [&](uint32_t (&v)[2][32], int cb) {
-                tmem_ld32(tS + lane_base + cb * 32, v[0]);
-                tmem_ld32(tS + lane_base + cb * 32 + 32, v[1]);
-                tmem_ld_wait();
-                if (!full) {
+            uint32_t sv[BN / 32][32];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int lo_c = rlo - (xt + 32 * (cb + u)), hi_c = rhi - (xt + 32 * (cb + u));
-                        uint32_t keep = 0u;
-                        if (hi_c > 0 && lo_c < 32) {
-                            const int b0 = lo_c > 0 ? lo_c : 0, b1 = hi_c < 32 ? hi_c : 32;
-                            keep = (b1 >= 32 ? 0xffffffffu : ((1u << b1) - 1u)) & ~((1u << b0) - 1u);
-                        }
+            for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + lane_base + c * 32, sv[c]);
+            tmem_ld_wait();
+            if (!full) {
 #pragma unroll
-                        for (int jj = 0; jj < 32; ++jj)
-                            if (!((keep >> jj) & 1u)) v[u][jj] = 0xff800000u;   // -inf
+                for (int c = 0; c < BN / 32; ++c) {
+                    const int lo_c = rlo - (xt + 32 * c), hi_c = rhi - (xt + 32 * c);
+                    uint32_t keep = 0u;
+                    if (hi_c > 0 && lo_c < 32) {
+                        const int b0 = lo_c > 0 ? lo_c : 0, b1 = hi_c < 32 ? hi_c : 32;
+                        keep = (b1 >= 32 ? 0xffffffffu : ((1u << b1) - 1u)) & ~((1u << b0) - 1u);
                     }
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        if (!((keep >> jj) & 1u)) sv[c][jj] = 0xff800000u;   // -inf
                 }
-            };
-            auto pair_max = [&](const uint32_t (&v)[2][32], float m) {
-                float m2[2] = {m, -INFINITY};
+            }
+            // row max: four independent chains of three-input maxima
+            float m4[BN / 32];
 #pragma unroll
-                for (int u = 0; u < 2; ++u)
+            for (int c = 0; c < BN / 32; ++c) {
+                m4[c] = -INFINITY;
 #pragma unroll
-                    for (int jj = 0; jj < 32; jj += 2)
-                        m2[u] = fmax3(m2[u], __uint_as_float(v[u][jj]), __uint_as_float(v[u][jj + 1]));
-                return fmaxf(m2[0], m2[1]);
-            };
-            // row max over columns [0, 64), then [64, 128) which stay in registers
-            uint32_t sv[2][32];
-            load_pair(sv, 0);
-            float mx = pair_max(sv, -INFINITY);
-            load_pair(sv, 2);
-            mx = pair_max(sv, mx);
+                for (int jj = 0; jj < 32; jj += 2)
+                    m4[c] = fmax3(m4[c], __uint_as_float(sv[c][jj]), __uint_as_float(sv[c][jj + 1]));
+            }
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             const float mx_s = mx * scale_log2;
             bool rescale = false;
             float alpha = 1.f;
@@ -312,7 +204,27 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 rescale = (l > 0.f);
                 m_ref = mx_s;
             }
-            // O_j is final for tiles < n here: S_j(n) was issued after PV_j(n-1)
+            l *= alpha;
+            // P = 2^(z scale log2e - m) as bf16 pairs: keys [32c, 32c+32) -> columns [16c, 16c+16)
+            const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            const float2 sc2 = make_float2(scale_log2, scale_log2), ng2 = make_float2(neg, neg);
+            float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const float2 z = __ffma2_rn(
+                        make_float2(__uint_as_float(sv[c][2 * jj]), __uint_as_float(sv[c][2 * jj + 1])), sc2, ng2);
+                    const float2 pv = make_float2(ex2(z.x), ex2(z.y));
+                    sum2[jj & 1] = __fadd2_rn(sum2[jj & 1], pv);
+                    pk[jj] = pack_bf16(pv.x, pv.y);
+                }
+                tmem_st16(tS + lane_base + c * 16, pk);
+            }
+            l += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
+            // O_j is final for tiles < n here (S_j(n) was issued after PV_j(n-1)); PV_j(n)
+            // waits for p_full below
             if (__any_sync(kAll, rescale)) {
                 const float f = rescale ? alpha : 1.f;
 #pragma unroll
@@ -325,31 +237,6 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     tmem_st32(tO + lane_base + c * 32, rr);
                 }
             }
-            l *= alpha;
-            // P = 2^(z scale log2e - m) as bf16 pairs: keys [64, 128) (in registers) to
-            // TMEM columns [64, 96), then keys [0, 64), re-read, to [0, 32)
-            const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            const float2 sc2 = make_float2(scale_log2, scale_log2), ng2 = make_float2(neg, neg);
-            float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            auto pair_exp = [&](const uint32_t (&v)[2][32], uint32_t col) {
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const float2 z = __ffma2_rn(
-                            make_float2(__uint_as_float(v[u][2 * jj]), __uint_as_float(v[u][2 * jj + 1])), sc2, ng2);
-                        const float2 pv = make_float2(ex2(z.x), ex2(z.y));
-                        sum2[jj & 1] = __fadd2_rn(sum2[jj & 1], pv);
-                        pk[jj] = pack_bf16(pv.x, pv.y);
-                    }
-                    tmem_st16(tS + lane_base + col + u * 16, pk);
-                }
-            };
-            pair_exp(sv, 64);
-            load_pair(sv, 0);
-            pair_exp(sv, 0);
-            l += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&sm.p_full[j]);
@@ -383,6 +270,117 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 lse_part[(int64_t(p) * Qn + row) * H + h] =
                     mine ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
+    } else {
+        warpgroup_reg_dealloc<kRegIssue>();
+        if (warp == kTmaWarp) {
+            // ------------------------------------------------------------ producer
+            if (lane == 0) {
+                int n = 0;
+                int64_t x0;
+                bool any = false;
+                while (it.next(x0)) {
+                    if (!any) {
+                        prefetch_tensormap(&map_k);
+                        prefetch_tensormap(&map_v);
+                        mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
+                        for (int j = 0; j < 2; ++j)
+                            for (int c = 0; c < NP; ++c)
+                                tma_load_2d(sm.q[j][c], &map_q, &sm.q_full, h * D + c * 64, (qt0 + j) * BM);
+                        any = true;
+                    }
+                    const int st = n % kStages;
+                    if (n >= kStages &&
+                        !mbar_wait(&sm.kv_empty[st], ((n - kStages) / kStages) & 1, wait_limit, &sm.abort_flag)) {
+                        abort_now();
+                        break;
+                    }
+                    if (*(volatile int*)&sm.abort_flag) break;
+                    mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+                    for (int c = 0; c < NP; ++c)
+                        tma_load_2d(sm.k[st][c], &map_k, &sm.k_full[st], h * D + c * 64, (int)x0);
+                    mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+                    for (int c = 0; c < NP; ++c)
+                        tma_load_2d(sm.v[st][c], &map_v, &sm.v_full[st], h * D + c * 64, (int)x0);
+                    ++n;
+                }
+                // every load this thread issued has landed before the block exits
+                if (any) mbar_wait(&sm.q_full, 0, kTeardownWait);
+                for (int st = 0; st < kStages && st < n; ++st) {
+                    const int last = st + ((n - 1 - st) / kStages) * kStages;   // last tile using stage st
+                    mbar_wait(&sm.k_full[st], (last / kStages) & 1, kTeardownWait);
+                    mbar_wait(&sm.v_full[st], (last / kStages) & 1, kTeardownWait);
+                }
+            }
+        } else if (warp == kMmaWarp) {
+            // ------------------------------------------------------------ MMA issuer
+            // The whole warp runs the schedule, so descriptors and counters are
+            // warp-uniform; one elected lane issues each group of MMAs and its commit.
+            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
+            constexpr uint32_t idO = idesc_bf16_f32(BM, D, 0, 1);
+            const int T = it.count();
+            auto wait = [&](uint64_t* bar, uint32_t parity) {
+                return mbar_wait_warp(bar, parity, wait_limit, &sm.abort_flag);
+            };
+            bool ok = T > 0;
+            bool issued = false;   // any MMA in flight to wait for before TMEM is freed
+            if (ok && stuck_test && !wait(&sm.stuck, 0)) ok = false;
+            if (ok) ok = wait(&sm.q_full, 0);
+            // shared-memory descriptors: the start-address field (bytes / 16) of a panel,
+            // stage or K step is an offset from the first one (every address < 256 KiB)
+            constexpr uint32_t kPanel = BN * 64 * 2 / 16, kStage = NP * kPanel;
+            const uint64_t dq = smem_desc(smem_u32(sm.q[0][0]), 16, 1024);
+            const uint64_t dk = smem_desc(smem_u32(sm.k[0][0]), 16, 1024);
+            const uint64_t dv = smem_desc(smem_u32(sm.v[0][0]), BN * 128, 1024);
+            auto issue_s = [&](int j, int n) -> bool {    // S_j = Q_j K_n^T -> TMEM [128 j, 128 j + 128)
+                const int st = n % kStages;
+                // K_n has landed once S_0(n) could be issued
+                if (j == 0 && !wait(&sm.k_full[st], (n / kStages) & 1)) return false;
+                tc_fence_after();
+                if (elect_one()) {
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+                        mma_ss(tmem + j * 128, dq + (j * kStage + off), dk + (st * kStage + off), idS, kk > 0);
+                    }
+                    mma_commit(&sm.s_full[j]);
+                }
+                __syncwarp();
+                issued = true;
+                return true;
+            };
+            auto issue_pv = [&](int j, int n) -> bool {   // O_j += P_j V_n (bf16 P_j over S_j)
+                const int st = n % kStages;
+                if (!wait(&sm.p_full[j], n & 1)) return false;
+                // V_n has landed once PV_0(n) could be issued
+                if (j == 0 && !wait(&sm.v_full[st], (n / kStages) & 1)) return false;
+                tc_fence_after();
+                if (elect_one()) {
+    #pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_ts(tmem + 256 + j * 128, tmem + j * 128 + kk * 8, dv + (st * kStage + kk * 128), idO,
+                               (n > 0 || kk > 0) ? 1u : 0u);
+                    if (j == 1) mma_commit(&sm.kv_empty[st]);   // both PVs of tile n have read V_n
+                }
+                __syncwarp();
+                return true;
+            };
+            if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
+            for (int n = 0; ok && n < T; ++n) {
+                // S_j(n+1) overwrites S_j right behind the PV_j(n) that reads P_j from it
+                if (!issue_pv(0, n)) { ok = false; break; }
+                if (n + 1 < T && !issue_s(0, n + 1)) { ok = false; break; }
+                if (!issue_pv(1, n)) { ok = false; break; }
+                if (n + 1 < T && !issue_s(1, n + 1)) { ok = false; break; }
+            }
+            if (!ok && T > 0 && lane == 0) abort_now();
+            // all MMAs the warp issued have completed before TMEM is freed
+            if (issued) {
+                if (elect_one()) mma_commit(&sm.mma_fin);
+                __syncwarp();
+                if (!mbar_wait_warp(&sm.mma_fin, 0, kTeardownWait) && lane == 0)
+                    skv::raise_status(status, SKV_ERR_TIMEOUT);
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -404,6 +402,11 @@ skv_status launch_fwd(const skv_problem& pb, const void* q, const void* k, const
     if (smem < 120 * 1024) smem = 120 * 1024;   // one block per SM: it owns all 512 TMEM columns
     auto kern = attn_fwd_tc_kernel<D>;
     SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    // the warpgroups' register split must fit the allocation the block launches with,
+    // or the softmax warpgroups' setmaxnreg.inc would never be granted
+    cudaFuncAttributes fa;
+    SKV_CUDA_CHECK(cudaFuncGetAttributes(&fa, kern));
+    if (fa.numRegs * kFwdThreads < 2 * 128 * kRegSoftmax + 128 * kRegIssue) return SKV_ERR_UNSUPPORTED;
     const int64_t n_qt = (Qn + BM - 1) / BM;
     int4* qtb = static_cast<int4*>(scratch);
     skv_status st = skv_tc::launch_qtile_bounds(pb, qtb, c);

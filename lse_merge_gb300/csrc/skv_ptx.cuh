@@ -248,6 +248,18 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Register reallocation between warpgroups (all four warps of a warpgroup
+// execute the same one): the launch-time allocation is redistributed, so the
+// sum over warpgroups must not exceed it.
+template <int N>
+__device__ __forceinline__ void warpgroup_reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void warpgroup_reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // three-input maximum (sm_100+), one instruction
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float y;
