@@ -425,6 +425,134 @@ def partitioned_backward(q, k, v, s, a, B: int, dO, rank_of_chunk, m: int, P: in
     return dq_parts.sum(axis=0), dk, dv, dq_parts
 
 
+# ---------------------------------------------------------------------------
+# The block-local term: each block's rows over the block's own B keys
+# ---------------------------------------------------------------------------
+#
+# Reading: besides its context window, block i attends bidirectionally to the B
+# tokens of its own block [Split-KV §3.1, Fig. 1 caption; the N B^2 term of
+# T_attn in §4.1].  Those tokens' keys and values are the drafter's own
+# projections of the block positions, so they arrive as two more tensors laid
+# out like q: k_blk, v_blk [Q, H, d], rows [iB, iB+B) belonging to block i.
+# They are disjoint from every context chunk, so their (o, l) is one more
+# partial of Eq. 4.
+
+def block_local_forward(q, k_blk, v_blk, B: int, scale: Optional[float] = None,
+                        heads: Optional[Sequence[int]] = None):
+    """Rows of block i over the block's own keys, unmasked:
+    z = scale q k_blk^T, l = log sum exp z, o = sum exp(z - l) v_blk.
+    Returns (o [Q,H,d], lse [Q,H]) float64."""
+    Qn, H, d = q.shape
+    N = Qn // B
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = np.zeros((Qn, H, d))
+    lse = np.full((Qn, H), NEG_INF)
+    for h in (range(H) if heads is None else heads):
+        for i in range(N):
+            rows = slice(i * B, (i + 1) * B)
+            z = scale * (_np64(q[rows, h, :]) @ _np64(k_blk[rows, h, :]).T)
+            e, ssum, l_rows, _ = _softmax_stats(z)
+            lse[rows, h] = l_rows
+            o[rows, h, :] = (e @ _np64(v_blk[rows, h, :])) / ssum[:, None]
+    return o, lse
+
+
+def full_mask_forward(q, k, v, k_blk, v_blk, s, a, B: int, scale: Optional[float] = None):
+    """The whole anchor mask at once, as its definition reads: block i's rows
+    see the context keys of W_i and their block's own B keys; one softmax over
+    that concatenated key set [Split-KV §3.1, Fig. 1].  Returns (o, lse)."""
+    s, a = _npi(s), _npi(a)
+    N = len(s)
+    Qn, H, d = q.shape
+    S = k.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = np.zeros((Qn, H, d))
+    lse = np.full((Qn, H), NEG_INF)
+    kv = _Heads(k, v)
+    for h in range(H):
+        kh, vh = kv.get(h)
+        for i in range(N):
+            rows = slice(i * B, (i + 1) * B)
+            keys = np.concatenate([kh, _np64(k_blk[rows, h, :])])
+            vals = np.concatenate([vh, _np64(v_blk[rows, h, :])])
+            visible = np.concatenate([mask_row(int(s[i]), int(a[i]), S), np.ones(B, dtype=bool)])
+            z = np.where(visible[None, :], scale * (_np64(q[rows, h, :]) @ keys.T), NEG_INF)
+            e, ssum, l_rows, _ = _softmax_stats(z)
+            lse[rows, h] = l_rows
+            o[rows, h, :] = (e @ vals) / ssum[:, None]
+    return o, lse
+
+
+def _given_backward(qb, kb, vb, gb, ob, lb, visible, scale):
+    """Gradients through one row block for keys kb/vb, given the merged output
+    ob and log-sum-exp lb of those rows: P = exp(z - l), D = dO . o,
+    dS = P (dP - D); returns (dq, dk, dv) of this key set."""
+    z = np.where(visible, scale * (qb @ kb.T), NEG_INF)
+    finite = np.isfinite(lb)
+    Pm = np.where(finite[:, None], np.exp(z - np.where(finite, lb, 0.0)[:, None]), 0.0)
+    dP = gb @ vb.T
+    D = (gb * ob).sum(axis=1)
+    dS = Pm * (dP - D[:, None])
+    return scale * (dS @ kb), scale * (dS.T @ qb), Pm.T @ gb
+
+
+def context_backward_given(q, k, v, s, a, B: int, dO, o, lse, scale: Optional[float] = None):
+    """The context part of the gradients of L = sum(dO * o) when o and lse are
+    the merged results of a larger key set (Alg. 1 line 15 in merged form):
+    P_rx = exp(z_rx - l_r) over W_i, D_r = dO_r . o_r, dS = P (dP - D).
+    With o, lse of the context alone this is ``attention_backward``.
+    Returns (dq, dk, dv)."""
+    s, a = _npi(s), _npi(a)
+    N = len(s)
+    Qn, H, d = q.shape
+    S = k.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o, lse, g = _np64(o), _np64(lse), _np64(dO)
+    dq = np.zeros((Qn, H, d))
+    dk = np.zeros((S, H, d))
+    dv = np.zeros((S, H, d))
+    kv = _Heads(k, v)
+    for h in range(H):
+        kh, vh = kv.get(h)
+        for i in range(N):
+            rows = slice(i * B, (i + 1) * B)
+            mrow = mask_row(int(s[i]), int(a[i]), S)[None, :]
+            gq, gk, gv = _given_backward(_np64(q[rows, h, :]), kh, vh, g[rows, h, :], o[rows, h, :],
+                                         lse[rows, h], mrow, scale)
+            dq[rows, h, :] = gq
+            dk[:, h, :] += gk
+            dv[:, h, :] += gv
+    return dq, dk, dv
+
+
+def block_local_backward(q, k_blk, v_blk, dO, o, lse, B: int, scale: Optional[float] = None):
+    """The block-local part of the same gradients: rows of block i over the
+    block's own keys with the merged o, lse.  Returns (dq_local [Q,H,d],
+    dk_blk [Q,H,d], dv_blk [Q,H,d]); the full dq is the context dq plus dq_local."""
+    Qn, H, d = q.shape
+    N = Qn // B
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o, lse, g = _np64(o), _np64(lse), _np64(dO)
+    dq = np.zeros((Qn, H, d))
+    dk = np.zeros((Qn, H, d))
+    dv = np.zeros((Qn, H, d))
+    allvis = np.ones((1, B), dtype=bool)
+    for h in range(H):
+        for i in range(N):
+            rows = slice(i * B, (i + 1) * B)
+            gq, gk, gv = _given_backward(_np64(q[rows, h, :]), _np64(k_blk[rows, h, :]),
+                                         _np64(v_blk[rows, h, :]), g[rows, h, :], o[rows, h, :],
+                                         lse[rows, h], allvis, scale)
+            dq[rows, h, :] = gq
+            dk[rows, h, :] = gk
+            dv[rows, h, :] = gv
+    return dq, dk, dv
+
+
 def merge_bytes(lse_part, d: int, out_elem_bytes: int) -> int:
     """Algorithmic HBM bytes of one LSE merge: every l_p (4 B), the o_p rows
     whose l_p is finite (d*4 B each), and the outputs o (d*out_elem_bytes) and
