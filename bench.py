@@ -122,15 +122,18 @@ class ClockSampler:
 
 
 def useful_pairs_per_head(s, a, B):
+    """Unmasked (query, context key) pairs of one head (the block-local B x B
+    pairs of each block are counted separately)."""
     return int(B * (a.long() - s.long()).clamp(min=0).sum().item())
 
 
 # ------------------------------------------------------------------ oracle legs
 
-def oracle_sample(w, inp, budget_s: float, block_offset: int = 0):
+def oracle_sample(w, inp, kb, vb, budget_s: float, block_offset: int = 0):
     """Times the CPU oracle (as it stands) on a bounded sample of the workload:
     forward (+ backward when the workload has one) of whole query blocks of one
-    head, until ~budget_s seconds of work.  Returns (TFLOP/s useful, desc)."""
+    head over the whole mask (context window and block-local keys), until
+    ~budget_s seconds of work.  Returns (TFLOP/s useful, desc)."""
     import oracle as orc
     N = w.N
     stride = max(1, N // 64)
@@ -140,10 +143,12 @@ def oracle_sample(w, inp, budget_s: float, block_offset: int = 0):
     pairs = 0
     done = []
     for i in order:
-        orc.attention_forward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, blocks=[i], heads=[head])
+        o, lse = orc.full_mask_forward(inp.q, inp.k, inp.v, kb, vb, inp.s, inp.a, w.B, blocks=[i], heads=[head])
         if w.backward:
-            orc.attention_backward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, inp.dO, blocks=[i], heads=[head])
-        pairs += w.B * max(0, int(inp.a[i]) - int(inp.s[i]))
+            orc.context_backward_given(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, inp.dO, o, lse,
+                                       blocks=[i], heads=[head])
+            orc.block_local_backward(inp.q, kb, vb, inp.dO, o, lse, w.B, blocks=[i], heads=[head])
+        pairs += w.B * max(0, int(inp.a[i]) - int(inp.s[i])) + w.B * w.B
         done.append(i)
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -166,15 +171,17 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    from workloads import WORKLOADS, make_inputs
+    from workloads import WORKLOADS, block_kv, make_inputs
     import torch
     w = WORKLOADS[args.workload]
     # the same draw as our arm (device generator when a GPU is present); the
     # oracle itself runs on the host cores only
-    inp = make_inputs(w, device="cuda" if torch.cuda.is_available() else "cpu")
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = make_inputs(w, device=gen_dev)
+    kb, vb = block_kv(w, device=gen_dev)
     per_step = []
     for t in range(args.warmup + args.steps):
-        tf, desc, dt = oracle_sample(w, inp, args.ref_step_s, block_offset=7 * t)
+        tf, desc, dt = oracle_sample(w, inp, kb, vb, args.ref_step_s, block_offset=7 * t)
         if t >= args.warmup:
             per_step.append((tf, dt, desc))
     value = statistics.mean(x[0] for x in per_step)
@@ -210,7 +217,7 @@ def run_ours(args):
         dist.barrier()
     import lse_merge_gb300 as skv
     from lse_merge_gb300 import _lib
-    from workloads import WORKLOADS, make_inputs
+    from workloads import WORKLOADS, block_kv, make_inputs
 
     lib = _lib.load()
     w = WORKLOADS[args.workload]
@@ -221,17 +228,21 @@ def run_ours(args):
     tdt = torch.float32 if w.dtype == "fp32" else torch.bfloat16
     s, a = inp.s.to(dev), inp.a.to(dev)
     q, k, v = inp.q, inp.k, inp.v
+    kb, vb = block_kv(w, device=str(dev))       # the block tokens' own keys / values
     dO = inp.dO if w.backward else None
     prob = skv.Problem(s, a, w.B, w.H, w.d, w.S, w.m, w.P, tdt)
     P, Q, H, d = w.P, w.Q, w.H, w.d
-    o_part = torch.empty(P, Q, H, d, dtype=torch.float32, device=dev)
-    lse_part = torch.empty(P, Q, H, dtype=torch.float32, device=dev)
+    # P rank partials + the block-local partial in slot P
+    o_part = torch.empty(P + 1, Q, H, d, dtype=torch.float32, device=dev)
+    lse_part = torch.empty(P + 1, Q, H, dtype=torch.float32, device=dev)
     o = torch.empty(Q, H, d, dtype=tdt, device=dev)
     lse = torch.empty(Q, H, dtype=torch.float32, device=dev)
     if w.backward:
         dq = torch.empty(Q, H, d, dtype=torch.float32, device=dev)
         dk = torch.empty(w.S, H, d, dtype=torch.float32, device=dev)
         dv = torch.empty(w.S, H, d, dtype=torch.float32, device=dev)
+        dkb = torch.empty(Q, H, d, dtype=torch.float32, device=dev)
+        dvb = torch.empty(Q, H, d, dtype=torch.float32, device=dev)
         ws_b = torch.empty(skv.workspace_bytes(prob, 1), dtype=torch.uint8, device=dev)
     ws_f = torch.empty(skv.workspace_bytes(prob, 0), dtype=torch.uint8, device=dev)
     costs = torch.empty(w.n_chunks, dtype=torch.int64, device=dev)
@@ -244,16 +255,19 @@ def run_ours(args):
         else:
             roc, _, _ = skv.contiguous_order(w.n_chunks, P, w.J, costs)
         if ev: ev[1].record()
-        skv.attn_fwd(prob, q, k, v, roc, o_part, lse_part, ws_f)
+        skv.attn_fwd(prob, q, k, v, roc, o_part[:P], lse_part[:P], ws_f)
+        skv.block_local_fwd(prob, q, kb, vb, o_part[P], lse_part[P])
         if ev: ev[2].record()
         skv.lse_merge(o_part, lse_part, o=o, lse=lse)
         if ev: ev[3].record()
         if w.backward:
             skv.attn_bwd(prob, q, k, v, o, lse, dO, roc, dq, dk, dv, ws_b)
+            skv.block_local_bwd(prob, q, kb, vb, o, lse, dO, dq, dkb, dvb)
         if ev: ev[4].record()
 
-    kt_names = ["attn_fwd_tc_kernel", "lse_merge_kernel", "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel"]
-    kt_buf = (ctypes.c_float * 4)()
+    kt_names = ["attn_fwd_tc_kernel", "lse_merge_kernel", "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel",
+                "block_local_fwd_kernel", "block_local_bwd_kernel"]
+    kt_buf = (ctypes.c_float * 6)()
     for _ in range(args.warmup):
         path()
     torch.cuda.synchronize()
@@ -299,16 +313,17 @@ def run_ours(args):
     lib.skv_set_kernel_timing(1)
     for t in range(max(3, min(args.steps, 5))):
         path()
-        if lib.skv_kernel_times(kt_buf, 4) == 0:
-            for i in range(4):
+        if lib.skv_kernel_times(kt_buf, 6) == 0:
+            for i in range(6):
                 if kt_buf[i] >= 0:
                     kt_ms[i].append(kt_buf[i])
     lib.skv_set_kernel_timing(0)
     torch.cuda.synchronize()
 
     pairs = useful_pairs_per_head(inp.s, inp.a, w.B) * H
-    fwd_flops = 4.0 * d * pairs
-    bwd_flops = 8.0 * d * pairs if w.backward else 0.0
+    blk_pairs = w.N * w.B * w.B * H                  # the block-local term's pairs
+    fwd_flops = 4.0 * d * (pairs + blk_pairs)
+    bwd_flops = 8.0 * d * (pairs + blk_pairs) if w.backward else 0.0
     step_flops = fwd_flops + bwd_flops
     value = step_flops * world / (ms * 1e-3) / 1e12
     pk, pk_kind = peaks()
@@ -316,13 +331,20 @@ def run_ours(args):
     hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     finite = int(torch.isfinite(lse_part).sum().item())
     out_b = 2 if tdt == torch.bfloat16 else 4
-    merge_bytes = P * Q * H * 4 + finite * d * 4 + Q * H * (d * out_b + 4)
+    merge_bytes = (P + 1) * Q * H * 4 + finite * d * 4 + Q * H * (d * out_b + 4)
     merge_gbs = merge_bytes / (ph["merge"] * 1e-3) / 1e9
     # credited (useful) FLOP of each main kernel per launch: forward 4d per pair;
     # the backward's 8d per pair (dV, dP, dQ, dK) is credited 6d to the dK/dV
     # kernel (dV, dP, dK) and 2d to the dQ kernel (dQ; its S and dP are recompute)
     credit = {"attn_fwd_tc_kernel": 4.0 * d * pairs, "attn_bwd_dkdv_tc_kernel": 6.0 * d * pairs,
               "attn_bwd_dq_tc_kernel": 2.0 * d * pairs}
+    # the block-local kernels are HBM-bound: their algorithmic bytes per launch
+    # (q, k_blk, v_blk in, o, lse out; backward also o, dO in and dq read+write,
+    # dk_blk, dv_blk out)
+    eb = 2 if tdt == torch.bfloat16 else 4
+    rows_h = Q * H
+    local_bytes = {"block_local_fwd_kernel": rows_h * (3 * d * eb + d * 4 + 4),
+                   "block_local_bwd_kernel": rows_h * (5 * d * eb + 4 + 2 * d * 4 + 2 * d * 4)}
     kernels = {}
     for i, nm in enumerate(kt_names):
         if kt_ms[i]:
@@ -330,6 +352,8 @@ def run_ours(args):
             kernels[nm] = {"ms": km}
             if nm in credit:
                 kernels[nm]["useful_tflops"] = credit[nm] / (km * 1e-3) / 1e12
+            if nm in local_bytes:
+                kernels[nm]["gbs"] = local_bytes[nm] / (km * 1e-3) / 1e9
     tensor_k = {k: v for k, v in kernels.items() if k in credit}
     dom = max(tensor_k, key=lambda k: tensor_k[k]["ms"]) if tensor_k else None
     dom_tf = tensor_k[dom]["useful_tflops"] if dom else 0.0
@@ -351,8 +375,10 @@ def run_ours(args):
         h_dq = torch.empty(Q, H, d, dtype=torch.float32, pin_memory=True)
         h_dk = torch.empty(w.S, H, d, dtype=torch.float32, pin_memory=True)
         h_dv = torch.empty(w.S, H, d, dtype=torch.float32, pin_memory=True)
-        h_in = [(x.cpu().pin_memory(), x) for x in (s, a, q, k, v, dO)]
-        h_out = [(o, h_o), (lse, h_lse), (dq, h_dq), (dk, h_dk), (dv, h_dv)]
+        h_dkb = torch.empty(Q, H, d, dtype=torch.float32, pin_memory=True)
+        h_dvb = torch.empty(Q, H, d, dtype=torch.float32, pin_memory=True)
+        h_in = [(x.cpu().pin_memory(), x) for x in (s, a, q, k, v, kb, vb, dO)]
+        h_out = [(o, h_o), (lse, h_lse), (dq, h_dq), (dk, h_dk), (dv, h_dv), (dkb, h_dkb), (dvb, h_dvb)]
         bi = sum(x.numel() * x.element_size() for x, _ in h_in)
         bo = sum(x.numel() * x.element_size() for x, _ in h_out)
 
@@ -382,7 +408,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, desc, _ = oracle_sample(w, inp, args.cpu_budget_s)
+        tf, desc, _ = oracle_sample(w, inp, kb, vb, args.cpu_budget_s)
         cpu = {"value": tf, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc}
 
     if rank == 0:
@@ -393,6 +419,7 @@ def run_ours(args):
             "config": {"workload": w.name, "b": w.n_samples, "S": w.S, "Q": w.Q, "B": w.B, "H": H, "d": d,
                        "m": w.m, "P": P, "J": w.J, "order": w.order,
                        "l2": "inputs larger than L2 (K+V alone exceed 129 MB)",
+                       "mask": "context windows + block-local B x B",
                        "parallelism": f"{world} independent replica(s)"},
             "pct_bf16_peak": {"measured_sustained": value / world / sustained,
                               "nominal_2250": value / world / 2250.0},

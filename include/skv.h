@@ -222,6 +222,38 @@ SKV_API skv_status skv_attn_bwd(const skv_problem* prob, const void* q, const vo
                         void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Block-local term of the anchor mask [Split-KV §3.1, Fig. 1 caption]: besides
+ * its context window W_i, each block's B tokens attend bidirectionally to one
+ * another.  Their keys and values (the block tokens' own projections) are
+ * given laid out like q.  The term is one more key set, disjoint from every
+ * context chunk, so its result is one more partial of Eq. 4: write it after
+ * the P rank partials (o_loc = o_part + P*Q*H*d, lse_loc = lse_part + P*Q*H)
+ * and merge P + 1 partials with skv_lse_merge to get the whole mask.
+ *   q, k_blk, v_blk  device [Q][H][d], dtype prob->dtype (Q = n_blocks * B)
+ *   o_loc            device float[Q][H][d], written
+ *   lse_loc          device float[Q][H], written (natural log)
+ * prob->B <= 32 and head_dim 64 or 128, else SKV_ERR_UNSUPPORTED; the anchor
+ * fields are not read.  Pointers 16-byte aligned (lse 4), else INVALID_ARG.
+ */
+SKV_API skv_status skv_block_local_fwd(const skv_problem* prob, const void* q, const void* k_blk, const void* v_blk,
+                                       float* o_loc, float* lse_loc, void* stream);
+
+/*
+ * Backward of the block-local term for L = sum(dO * o) of the whole mask,
+ * with o and lse the MERGED results (context ranks + this term), the same
+ * merged form as skv_attn_bwd [Alg. 1 line 15]: P = exp(z - lse), D = dO . o,
+ * dS = P (dP - D).
+ *   o                device [Q][H][d], dtype prob->dtype; lse device float[Q][H]
+ *   dq               device float[Q][H][d], ACCUMULATED: call after
+ *                    skv_attn_bwd (which writes the context part) on the same
+ *                    stream, and dq holds the whole-mask gradient
+ *   dk_blk, dv_blk   device float[Q][H][d], written
+ */
+SKV_API skv_status skv_block_local_bwd(const skv_problem* prob, const void* q, const void* k_blk, const void* v_blk,
+                                       const void* o, const float* lse, const void* dO, float* dq, float* dk_blk,
+                                       float* dv_blk, void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device (SKV_ERR_BAD_ANCHORS, SKV_ERR_TIMEOUT, SKV_ERR_INVALID_ARG
  * raised by kernels), or SKV_ERR_CUDA if the stream reports a CUDA error.
@@ -253,7 +285,8 @@ SKV_API uint64_t skv_launch_count(void);
  * Measurement hook.  skv_set_kernel_timing(1) makes the library record a
  * CUDA event pair on the launching stream around each of its main kernels:
  * slot 0 the forward attention kernel, 1 the LSE merge, 2 the backward dK/dV
- * kernel, 3 the backward dQ kernel (tensor-core path).  skv_kernel_times
+ * kernel, 3 the backward dQ kernel (tensor-core path), 4 and 5 the
+ * block-local forward and backward.  skv_kernel_times
  * waits for the last recorded pair of each of the first n slots and writes
  * its duration in milliseconds (-1 where nothing was recorded since the
  * previous read).  Off by default; the events are created on first use.

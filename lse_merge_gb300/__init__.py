@@ -21,7 +21,7 @@ from ._lib import SKV_BF16, SKV_FP32, SkvProblem
 
 __all__ = ["SkvError", "Problem", "chunk_costs", "lpt_order", "contiguous_order", "zigzag_loads",
            "workspace_bytes", "attn_fwd", "attn_fwd_static", "lse_merge", "attn_bwd", "stream_status", "set_wait_limit",
-           "forward", "plan"]
+           "forward", "plan", "block_local_fwd", "block_local_bwd"]
 
 
 class SkvError(RuntimeError):
@@ -191,6 +191,29 @@ def attn_bwd(prob: Problem, q, k, v, o, lse, dO, rank_of_chunk, dq=None, dk=None
                                     _ptr(rank_of_chunk), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
                                     _stream()), "skv_attn_bwd")
     return dq, dk, dv
+
+
+def block_local_fwd(prob: Problem, q, k_blk, v_blk, o_loc=None, lse_loc=None):
+    """(o_loc fp32 [Q,H,d], lse_loc fp32 [Q,H]): each block's rows over its own B keys,
+    one more partial for lse_merge."""
+    dev = q.device
+    o_loc = torch.empty(prob.Q, prob.H, prob.d, dtype=torch.float32, device=dev) if o_loc is None else o_loc
+    lse_loc = torch.empty(prob.Q, prob.H, dtype=torch.float32, device=dev) if lse_loc is None else lse_loc
+    _check(_lib.load().skv_block_local_fwd(prob.ref(), _ptr(q), _ptr(k_blk), _ptr(v_blk), _ptr(o_loc),
+                                           _ptr(lse_loc), _stream()), "skv_block_local_fwd")
+    return o_loc, lse_loc
+
+
+def block_local_bwd(prob: Problem, q, k_blk, v_blk, o, lse, dO, dq, dk_blk=None, dv_blk=None):
+    """Adds the block-local part to dq (fp32, holding the context part) and returns
+    (dq, dk_blk, dv_blk); o, lse are the merged results of the whole mask."""
+    dev = q.device
+    dk_blk = torch.empty(prob.Q, prob.H, prob.d, dtype=torch.float32, device=dev) if dk_blk is None else dk_blk
+    dv_blk = torch.empty(prob.Q, prob.H, prob.d, dtype=torch.float32, device=dev) if dv_blk is None else dv_blk
+    _check(_lib.load().skv_block_local_bwd(prob.ref(), _ptr(q), _ptr(k_blk), _ptr(v_blk), _ptr(o), _ptr(lse),
+                                           _ptr(dO), _ptr(dq), _ptr(dk_blk), _ptr(dv_blk), _stream()),
+           "skv_block_local_bwd")
+    return dq, dk_blk, dv_blk
 
 
 def stream_status() -> int:

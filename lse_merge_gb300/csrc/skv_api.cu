@@ -289,6 +289,38 @@ skv_status skv_attn_bwd(const skv_problem* pb_in, const void* q, const void* k, 
     return skv_internal::launch_dq_sum(w.dq_part, pb.P, rows, pb.head_dim, dq, c);
 }
 
+skv_status skv_block_local_fwd(const skv_problem* pb_in, const void* q, const void* k_blk, const void* v_blk,
+                               float* o_loc, float* lse_loc, void* stream) {
+    skv_status st = validate(pb_in, false);
+    if (st != SKV_OK) return st;
+    if (pb_in->head_dim != 64 && pb_in->head_dim != 128) return SKV_ERR_UNSUPPORTED;
+    const skv_problem pb = normalized(pb_in);
+    if (!skv_internal::block_local_supported(pb)) return SKV_ERR_UNSUPPORTED;
+    if (pb.n_blocks == 0) return SKV_OK;
+    if (bad_ptr(q, 16) || bad_ptr(k_blk, 16) || bad_ptr(v_blk, 16) || bad_ptr(o_loc, 16) || bad_ptr(lse_loc, 4))
+        return SKV_ERR_INVALID_ARG;
+    skv_host::Ctx c;
+    if ((st = skv_host::get_ctx(stream, c)) != SKV_OK) return st;
+    return skv_internal::launch_block_local_fwd(pb, q, k_blk, v_blk, o_loc, lse_loc, c);
+}
+
+skv_status skv_block_local_bwd(const skv_problem* pb_in, const void* q, const void* k_blk, const void* v_blk,
+                               const void* o, const float* lse, const void* dO, float* dq, float* dk_blk,
+                               float* dv_blk, void* stream) {
+    skv_status st = validate(pb_in, false);
+    if (st != SKV_OK) return st;
+    if (pb_in->head_dim != 64 && pb_in->head_dim != 128) return SKV_ERR_UNSUPPORTED;
+    const skv_problem pb = normalized(pb_in);
+    if (!skv_internal::block_local_supported(pb)) return SKV_ERR_UNSUPPORTED;
+    if (pb.n_blocks == 0) return SKV_OK;
+    if (bad_ptr(q, 16) || bad_ptr(k_blk, 16) || bad_ptr(v_blk, 16) || bad_ptr(o, 16) || bad_ptr(lse, 4) ||
+        bad_ptr(dO, 16) || bad_ptr(dq, 16) || bad_ptr(dk_blk, 16) || bad_ptr(dv_blk, 16))
+        return SKV_ERR_INVALID_ARG;
+    skv_host::Ctx c;
+    if ((st = skv_host::get_ctx(stream, c)) != SKV_OK) return st;
+    return skv_internal::launch_block_local_bwd(pb, q, k_blk, v_blk, o, lse, dO, dq, dk_blk, dv_blk, c);
+}
+
 skv_status skv_stream_status(void* stream) {
     skv_host::Ctx c;
     skv_status st = skv_host::get_ctx(stream, c);

@@ -65,7 +65,8 @@ void note_launch(int n = 1);
 
 // Optional per-kernel CUDA-event timing (skv_set_kernel_timing): slots of the
 // main kernels; begin/end record events on the launching stream when enabled.
-enum TimerSlot { kTimeFwd = 0, kTimeMerge = 1, kTimeBwdKV = 2, kTimeBwdQ = 3, kTimeSlots = 4 };
+enum TimerSlot { kTimeFwd = 0, kTimeMerge = 1, kTimeBwdKV = 2, kTimeBwdQ = 3, kTimeLocalFwd = 4, kTimeLocalBwd = 5,
+                 kTimeSlots = 6 };
 void timer_begin(int slot, cudaStream_t stream);
 void timer_end(int slot, cudaStream_t stream);
 

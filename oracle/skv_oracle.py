@@ -458,10 +458,12 @@ def block_local_forward(q, k_blk, v_blk, B: int, scale: Optional[float] = None,
     return o, lse
 
 
-def full_mask_forward(q, k, v, k_blk, v_blk, s, a, B: int, scale: Optional[float] = None):
+def full_mask_forward(q, k, v, k_blk, v_blk, s, a, B: int, scale: Optional[float] = None,
+                      blocks: Optional[Sequence[int]] = None, heads: Optional[Sequence[int]] = None):
     """The whole anchor mask at once, as its definition reads: block i's rows
     see the context keys of W_i and their block's own B keys; one softmax over
-    that concatenated key set [Split-KV §3.1, Fig. 1].  Returns (o, lse)."""
+    that concatenated key set [Split-KV §3.1, Fig. 1].  ``blocks``/``heads``
+    restrict the rows/heads computed (others stay 0/-inf).  Returns (o, lse)."""
     s, a = _npi(s), _npi(a)
     N = len(s)
     Qn, H, d = q.shape
@@ -471,9 +473,9 @@ def full_mask_forward(q, k, v, k_blk, v_blk, s, a, B: int, scale: Optional[float
     o = np.zeros((Qn, H, d))
     lse = np.full((Qn, H), NEG_INF)
     kv = _Heads(k, v)
-    for h in range(H):
+    for h in (range(H) if heads is None else heads):
         kh, vh = kv.get(h)
-        for i in range(N):
+        for i in (range(N) if blocks is None else blocks):
             rows = slice(i * B, (i + 1) * B)
             keys = np.concatenate([kh, _np64(k_blk[rows, h, :])])
             vals = np.concatenate([vh, _np64(v_blk[rows, h, :])])
@@ -498,12 +500,13 @@ def _given_backward(qb, kb, vb, gb, ob, lb, visible, scale):
     return scale * (dS @ kb), scale * (dS.T @ qb), Pm.T @ gb
 
 
-def context_backward_given(q, k, v, s, a, B: int, dO, o, lse, scale: Optional[float] = None):
+def context_backward_given(q, k, v, s, a, B: int, dO, o, lse, scale: Optional[float] = None,
+                           blocks: Optional[Sequence[int]] = None, heads: Optional[Sequence[int]] = None):
     """The context part of the gradients of L = sum(dO * o) when o and lse are
     the merged results of a larger key set (Alg. 1 line 15 in merged form):
     P_rx = exp(z_rx - l_r) over W_i, D_r = dO_r . o_r, dS = P (dP - D).
     With o, lse of the context alone this is ``attention_backward``.
-    Returns (dq, dk, dv)."""
+    ``blocks``/``heads`` restrict which query rows contribute.  Returns (dq, dk, dv)."""
     s, a = _npi(s), _npi(a)
     N = len(s)
     Qn, H, d = q.shape
@@ -515,9 +518,9 @@ def context_backward_given(q, k, v, s, a, B: int, dO, o, lse, scale: Optional[fl
     dk = np.zeros((S, H, d))
     dv = np.zeros((S, H, d))
     kv = _Heads(k, v)
-    for h in range(H):
+    for h in (range(H) if heads is None else heads):
         kh, vh = kv.get(h)
-        for i in range(N):
+        for i in (range(N) if blocks is None else blocks):
             rows = slice(i * B, (i + 1) * B)
             mrow = mask_row(int(s[i]), int(a[i]), S)[None, :]
             gq, gk, gv = _given_backward(_np64(q[rows, h, :]), kh, vh, g[rows, h, :], o[rows, h, :],
@@ -528,7 +531,8 @@ def context_backward_given(q, k, v, s, a, B: int, dO, o, lse, scale: Optional[fl
     return dq, dk, dv
 
 
-def block_local_backward(q, k_blk, v_blk, dO, o, lse, B: int, scale: Optional[float] = None):
+def block_local_backward(q, k_blk, v_blk, dO, o, lse, B: int, scale: Optional[float] = None,
+                         blocks: Optional[Sequence[int]] = None, heads: Optional[Sequence[int]] = None):
     """The block-local part of the same gradients: rows of block i over the
     block's own keys with the merged o, lse.  Returns (dq_local [Q,H,d],
     dk_blk [Q,H,d], dv_blk [Q,H,d]); the full dq is the context dq plus dq_local."""
@@ -541,8 +545,8 @@ def block_local_backward(q, k_blk, v_blk, dO, o, lse, B: int, scale: Optional[fl
     dk = np.zeros((Qn, H, d))
     dv = np.zeros((Qn, H, d))
     allvis = np.ones((1, B), dtype=bool)
-    for h in range(H):
-        for i in range(N):
+    for h in (range(H) if heads is None else heads):
+        for i in (range(N) if blocks is None else blocks):
             rows = slice(i * B, (i + 1) * B)
             gq, gk, gv = _given_backward(_np64(q[rows, h, :]), _np64(k_blk[rows, h, :]),
                                          _np64(v_blk[rows, h, :]), g[rows, h, :], o[rows, h, :],

@@ -14,7 +14,10 @@ ascending inside the sample; blocks are ordered by (sample, anchor).  Block i of
 sample u has s_i = u*L (the sample start) and a_i its anchor.
 
 Draw order for one workload (one torch CPU generator seeded once):
-anchors (sample by sample) -> q -> k -> v -> dO.
+anchors (sample by sample) -> q -> k -> v -> dO.  The block tokens' own keys
+and values (the block-local term of the mask) come from a second generator
+seeded with seed + 1000003, so adding them changes none of the draws above:
+k_blk -> v_blk, [Q, H, d], distributed like q.
 """
 from __future__ import annotations
 
@@ -167,6 +170,27 @@ def make_inputs(w: Workload, with_grad: Optional[bool] = None, pin: bool = False
     want = w.backward if with_grad is None else with_grad
     dO = draw((w.Q, w.H, w.d), w.do_std) if want else None
     return Inputs(w, s, a, q, k, v, dO)
+
+
+def block_kv(w: Workload, device: str = "cpu"):
+    """(k_blk, v_blk) [Q, H, d]: the block tokens' own keys and values for the
+    block-local term, drawn like q from their own seeded generator."""
+    tdt = torch.float32 if w.dtype == "fp32" else torch.bfloat16
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed + 1000003)
+    out = []
+    for _ in range(2):
+        x = torch.empty(w.Q, w.H, w.d, dtype=tdt, device=device)
+        flat = x.view(-1)
+        step = 1 << 26
+        for i in range(0, flat.numel(), step):
+            n = min(step, flat.numel() - i)
+            r = torch.randn(n, generator=g, dtype=torch.float32, device=device)
+            if w.qkv_std != 1.0:
+                r.mul_(w.qkv_std)
+            flat[i:i + n] = r.to(tdt)
+        out.append(x)
+    return out[0], out[1]
 
 
 def random_small(seed: int, n_samples: int, sample_len: int, anchors_per_sample: int,
