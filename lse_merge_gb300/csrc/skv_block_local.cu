@@ -36,6 +36,33 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 constexpr int kWarps = 4;   // warps per (block, head) CTA
 
+// 8 consecutive elements as floats (d is a multiple of 8, rows 16-byte aligned)
+__device__ __forceinline__ void ld8(const __nv_bfloat16* p, int64_t i, float (&x)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void ld8(const float* p, int64_t i, float (&x)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p + i), b = *reinterpret_cast<const float4*>(p + i + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+// rows [iB, iB+B) of head h of a [Q][H][d] tensor into shared rows of stride `stride`
+template <typename T>
+__device__ __forceinline__ void stage_rows(const T* src, int i, int B, int H, int h, int d, float* dst, int stride) {
+    const int per_row = d / 8;
+    for (int e = threadIdx.x; e < B * per_row; e += blockDim.x) {
+        const int r = e / per_row, t = (e - r * per_row) * 8;
+        float x[8];
+        ld8(src, ((int64_t(i) * B + r) * H + h) * d + t, x);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) dst[r * stride + t + u] = x[u];
+    }
+}
+
 // shared floats of one CTA
 __host__ __device__ inline int fwd_floats(int B, int d) { return 2 * B * (d + 1) + B * d + B * 32; }
 __host__ __device__ inline int bwd_floats(int B, int d) { return 4 * B * (d + 1) + 2 * B * 32 + 32; }
@@ -55,21 +82,20 @@ block_local_fwd_kernel(const T* __restrict__ q, const T* __restrict__ kb, const 
     float* sk = sq + B * dp;
     float* sv = sk + B * dp;
     float* sp = sv + B * d;   // [B][32] weights of each row
-    for (int e = threadIdx.x; e < B * d; e += blockDim.x) {
-        const int r = e / d, t = e - r * d;
-        const int64_t g = ((int64_t(i) * B + r) * H + h) * d + t;
-        sq[r * dp + t] = ld(q, g);
-        sk[r * dp + t] = ld(kb, g);
-        sv[r * d + t] = ld(vb, g);
-    }
+    stage_rows(q, i, B, H, h, d, sq, dp);
+    stage_rows(kb, i, B, H, h, d, sk, dp);
+    stage_rows(vb, i, B, H, h, d, sv, d);
     __syncthreads();
     for (int r = warp; r < B; r += kWarps) {
-        float z = -INFINITY;   // log2 units
-        if (lane < B) {
-            float acc = 0.f;
-            for (int t = 0; t < d; ++t) acc = fmaf(sq[r * dp + t], sk[lane * dp + t], acc);
-            z = acc * scale_log2;
-        }
+        // key j on lane j (B > 16) or on lanes j and j + 16, each over half of d
+        const bool two = B <= 16;
+        const int j = two ? (lane & 15) : lane;
+        const int t0 = two ? (lane >> 4) * (d / 2) : 0, t1 = two ? t0 + d / 2 : d;
+        float acc = 0.f;
+        if (j < B)
+            for (int t = t0; t < t1; ++t) acc = fmaf(sq[r * dp + t], sk[j * dp + t], acc);
+        if (two) acc += __shfl_xor_sync(kAll, acc, 16);
+        const float z = (j < B && (!two || lane < 16)) ? acc * scale_log2 : -INFINITY;   // log2 units
         const float mx = warp_max(z);
         const float p = lane < B ? exp2f(z - mx) : 0.f;
         const float sum = warp_sum(p);
@@ -105,14 +131,10 @@ block_local_bwd_kernel(const T* __restrict__ q, const T* __restrict__ kb, const 
     float* sp = sg + B * dp;     // [B][32] P
     float* ss = sp + B * 32;     // [B][32] dS
     float* sD = ss + B * 32;     // D per row
-    for (int e = threadIdx.x; e < B * d; e += blockDim.x) {
-        const int r = e / d, t = e - r * d;
-        const int64_t g = ((int64_t(i) * B + r) * H + h) * d + t;
-        sq[r * dp + t] = ld(q, g);
-        sk[r * dp + t] = ld(kb, g);
-        sv[r * dp + t] = ld(vb, g);
-        sg[r * dp + t] = ld(dO, g);
-    }
+    stage_rows(q, i, B, H, h, d, sq, dp);
+    stage_rows(kb, i, B, H, h, d, sk, dp);
+    stage_rows(vb, i, B, H, h, d, sv, dp);
+    stage_rows(dO, i, B, H, h, d, sg, dp);
     for (int r = warp; r < B; r += kWarps) {   // D_r = dO_r . o_r
         const int64_t g0 = ((int64_t(i) * B + r) * H + h) * d;
         float part = 0.f;
@@ -124,18 +146,29 @@ block_local_bwd_kernel(const T* __restrict__ q, const T* __restrict__ kb, const 
     const float scale_log2 = scale * kLog2e;
     for (int r = warp; r < B; r += kWarps) {
         const float l = lse[(int64_t(i) * B + r) * H + h];
-        float P = 0.f, dS = 0.f;
-        if (lane < B && isfinite(l)) {
-            float zs = 0.f, dpv = 0.f;
-            for (int t = 0; t < d; ++t) {
-                zs = fmaf(sq[r * dp + t], sk[lane * dp + t], zs);
-                dpv = fmaf(sg[r * dp + t], sv[lane * dp + t], dpv);
+        // key j on lane j (B > 16) or on lanes j and j + 16, each over half of d
+        const bool two = B <= 16;
+        const int j = two ? (lane & 15) : lane;
+        const int t0 = two ? (lane >> 4) * (d / 2) : 0, t1 = two ? t0 + d / 2 : d;
+        float zs = 0.f, dpv = 0.f;
+        if (j < B)
+            for (int t = t0; t < t1; ++t) {
+                zs = fmaf(sq[r * dp + t], sk[j * dp + t], zs);
+                dpv = fmaf(sg[r * dp + t], sv[j * dp + t], dpv);
             }
+        if (two) {
+            zs += __shfl_xor_sync(kAll, zs, 16);
+            dpv += __shfl_xor_sync(kAll, dpv, 16);
+        }
+        float P = 0.f, dS = 0.f;
+        if (j < B && isfinite(l)) {
             P = exp2f(zs * scale_log2 - l * kLog2e);
             dS = P * (dpv - sD[r]);
         }
-        sp[r * 32 + lane] = P;
-        ss[r * 32 + lane] = dS;
+        if (!two || lane < 16) {
+            sp[r * 32 + j] = P;
+            ss[r * 32 + j] = dS;
+        }
     }
     __syncthreads();
     for (int r = warp; r < B; r += kWarps) {   // dq rows
