@@ -129,11 +129,10 @@ def useful_pairs_per_head(s, a, B):
 
 # ------------------------------------------------------------------ oracle legs
 
-def oracle_sample(w, inp, kb, vb, budget_s: float, block_offset: int = 0):
+def oracle_sample(w, inp, budget_s: float, block_offset: int = 0):
     """Times the CPU oracle (as it stands) on a bounded sample of the workload:
     forward (+ backward when the workload has one) of whole query blocks of one
-    head over the whole mask (context window and block-local keys), until
-    ~budget_s seconds of work.  Returns (TFLOP/s useful, desc)."""
+    head, until ~budget_s seconds of work.  Returns (TFLOP/s useful, desc)."""
     import oracle as orc
     N = w.N
     stride = max(1, N // 64)
@@ -143,12 +142,10 @@ def oracle_sample(w, inp, kb, vb, budget_s: float, block_offset: int = 0):
     pairs = 0
     done = []
     for i in order:
-        o, lse = orc.full_mask_forward(inp.q, inp.k, inp.v, kb, vb, inp.s, inp.a, w.B, blocks=[i], heads=[head])
+        orc.attention_forward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, blocks=[i], heads=[head])
         if w.backward:
-            orc.context_backward_given(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, inp.dO, o, lse,
-                                       blocks=[i], heads=[head])
-            orc.block_local_backward(inp.q, kb, vb, inp.dO, o, lse, w.B, blocks=[i], heads=[head])
-        pairs += w.B * max(0, int(inp.a[i]) - int(inp.s[i])) + w.B * w.B
+            orc.attention_backward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, inp.dO, blocks=[i], heads=[head])
+        pairs += w.B * max(0, int(inp.a[i]) - int(inp.s[i]))
         done.append(i)
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -167,21 +164,79 @@ def blas_threads():
         return os.cpu_count() or 1
 
 
+def run_planner_study(args):
+    """Planner quality and latency on the shapes of the pages' planner study
+    [Split-KV §5.5, Figs. 9 and 10]: b = 4 samples with a 1:3 prompt-to-response
+    split, anchors at one per 256 context positions in the response (the
+    density of the packed workload), B = 16, m = 4096.  Context per sample
+    16k..256k at P = 8, then P = 8..64 at 256k.  For LPT, contiguous ("no
+    balance") and Zigzag on the GPU: rho = max_p W_p / mean_p W_p with
+    W_p = C_p + (N/P) B^2, and the latency of costs + LPT (CUDA events, warm).
+    Prints one JSON line per shape."""
+    import torch
+    import lse_merge_gb300 as skv
+    from lse_merge_gb300.build import build
+    from workloads import Workload, draw_anchors
+    build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    shapes = [(L, 8) for L in (16384, 32768, 65536, 131072, 262144)] + [(262144, P) for P in (16, 32, 64)]
+    B, m, b = 16, 4096, 4
+    for L, P in shapes:
+        A = L // 256
+        w = Workload(f"planner_{L // 1024}k_P{P}", 77, b, L, A, L // 4, L, B, 1, 128, m, P, "bf16", 0.5, 1.0,
+                     "lpt", False)
+        g = torch.Generator().manual_seed(w.seed)
+        s, a = draw_anchors(w, g)
+        s, a = s.to(dev), a.to(dev)
+        prob = skv.Problem(s, a, B, 1, 128, w.S, m, P, torch.bfloat16)
+        n = w.n_chunks
+        costs = torch.empty(n, dtype=torch.int64, device=dev)
+        starts = torch.arange(b, dtype=torch.int32, device=dev) * L
+        lens = torch.full((b,), L, dtype=torch.int32, device=dev)
+        D = (w.N / P) * B * B
+
+        def rho(load):
+            W = load.double() + D
+            return float(W.max() / W.mean())
+
+        for _ in range(3):                      # warm-up
+            skv.chunk_costs(prob, costs)
+            skv.lpt_order(costs, P, w.J)
+        reps = 20
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            skv.chunk_costs(prob, costs)
+            _, _, load_lpt = skv.lpt_order(costs, P, w.J)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        _, _, load_con = skv.contiguous_order(n, P, w.J, costs)
+        load_zz = skv.zigzag_loads(prob, starts, lens)
+        if skv.stream_status() != 0:
+            raise RuntimeError("device status set by the planners")
+        print(json.dumps({"study": "planners", "shape": {"context_per_sample": L, "samples": b, "P": P,
+                                                         "anchors_per_sample": A, "B": B, "m": m, "J": w.J},
+                          "imbalance_pct": {"lpt": 100 * (rho(load_lpt) - 1), "contiguous": 100 * (rho(load_con) - 1),
+                                            "zigzag": 100 * (rho(load_zz) - 1)},
+                          "plan_ms_costs_plus_lpt": ms}), flush=True)
+    return 0
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    from workloads import WORKLOADS, block_kv, make_inputs
+    from workloads import WORKLOADS, make_inputs
     import torch
     w = WORKLOADS[args.workload]
     # the same draw as our arm (device generator when a GPU is present); the
     # oracle itself runs on the host cores only
-    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
-    inp = make_inputs(w, device=gen_dev)
-    kb, vb = block_kv(w, device=gen_dev)
+    inp = make_inputs(w, device="cuda" if torch.cuda.is_available() else "cpu")
     per_step = []
     for t in range(args.warmup + args.steps):
-        tf, desc, dt = oracle_sample(w, inp, kb, vb, args.ref_step_s, block_offset=7 * t)
+        tf, desc, dt = oracle_sample(w, inp, args.ref_step_s, block_offset=7 * t)
         if t >= args.warmup:
             per_step.append((tf, dt, desc))
     value = statistics.mean(x[0] for x in per_step)
@@ -232,7 +287,7 @@ def run_ours(args):
     dO = inp.dO if w.backward else None
     prob = skv.Problem(s, a, w.B, w.H, w.d, w.S, w.m, w.P, tdt)
     P, Q, H, d = w.P, w.Q, w.H, w.d
-    # P rank partials + the block-local partial in slot P
+    # P rank partials (+ slot P for the block-local partial of the separate pass)
     o_part = torch.empty(P + 1, Q, H, d, dtype=torch.float32, device=dev)
     lse_part = torch.empty(P + 1, Q, H, dtype=torch.float32, device=dev)
     o = torch.empty(Q, H, d, dtype=tdt, device=dev)
@@ -256,14 +311,23 @@ def run_ours(args):
             roc, _, _ = skv.contiguous_order(w.n_chunks, P, w.J, costs)
         if ev: ev[1].record()
         skv.attn_fwd(prob, q, k, v, roc, o_part[:P], lse_part[:P], ws_f)
-        skv.block_local_fwd(prob, q, kb, vb, o_part[P], lse_part[P])
         if ev: ev[2].record()
-        skv.lse_merge(o_part, lse_part, o=o, lse=lse)
+        skv.lse_merge(o_part[:P], lse_part[:P], o=o, lse=lse)
         if ev: ev[3].record()
         if w.backward:
             skv.attn_bwd(prob, q, k, v, o, lse, dO, roc, dq, dk, dv, ws_b)
-            skv.block_local_bwd(prob, q, kb, vb, o, lse, dO, dq, dkb, dvb)
         if ev: ev[4].record()
+        return roc
+
+    def local_pass(roc):
+        # the block-local term of the mask (the first widening past the context
+        # path): its partial in slot P, the P + 1 merge, its backward on top of dq
+        skv.attn_fwd(prob, q, k, v, roc, o_part[:P], lse_part[:P], ws_f)
+        skv.block_local_fwd(prob, q, kb, vb, o_part[P], lse_part[P])
+        skv.lse_merge(o_part, lse_part, o=o, lse=lse)
+        if w.backward:
+            skv.attn_bwd(prob, q, k, v, o, lse, dO, roc, dq, dk, dv, ws_b)
+            skv.block_local_bwd(prob, q, kb, vb, o, lse, dO, dq, dkb, dvb)
 
     kt_names = ["attn_fwd_tc_kernel", "lse_merge_kernel", "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel",
                 "block_local_fwd_kernel", "block_local_bwd_kernel"]
@@ -311,19 +375,37 @@ def run_ours(args):
     # stream, read after each step of a separate pass of the same steps
     kt_ms = [[] for _ in kt_names]
     lib.skv_set_kernel_timing(1)
-    for t in range(max(3, min(args.steps, 5))):
-        path()
+    n_kt = max(3, min(args.steps, 5))
+    for t in range(n_kt):
+        roc_t = path()
+        if lib.skv_kernel_times(kt_buf, 4) == 0:
+            for i in range(4):
+                if kt_buf[i] >= 0:
+                    kt_ms[i].append(kt_buf[i])
+        local_pass(roc_t)
         if lib.skv_kernel_times(kt_buf, 6) == 0:
-            for i in range(6):
+            for i in (4, 5):
                 if kt_buf[i] >= 0:
                     kt_ms[i].append(kt_buf[i])
     lib.skv_set_kernel_timing(0)
     torch.cuda.synchronize()
+    # the whole mask (context + block-local term) as one step, outside the headline
+    roc_l = path()
+    local_pass(roc_l)
+    torch.cuda.synchronize()
+    if skv.stream_status() != 0:
+        raise RuntimeError("device status set by the block-local pass")
+    l_s, l_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l_s.record()
+    for _ in range(n_kt):
+        local_pass(roc_l)
+    l_e.record()
+    torch.cuda.synchronize()
+    whole_ms = l_s.elapsed_time(l_e) / n_kt
 
     pairs = useful_pairs_per_head(inp.s, inp.a, w.B) * H
-    blk_pairs = w.N * w.B * w.B * H                  # the block-local term's pairs
-    fwd_flops = 4.0 * d * (pairs + blk_pairs)
-    bwd_flops = 8.0 * d * (pairs + blk_pairs) if w.backward else 0.0
+    fwd_flops = 4.0 * d * pairs
+    bwd_flops = 8.0 * d * pairs if w.backward else 0.0
     step_flops = fwd_flops + bwd_flops
     value = step_flops * world / (ms * 1e-3) / 1e12
     pk, pk_kind = peaks()
@@ -331,7 +413,7 @@ def run_ours(args):
     hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     finite = int(torch.isfinite(lse_part).sum().item())
     out_b = 2 if tdt == torch.bfloat16 else 4
-    merge_bytes = (P + 1) * Q * H * 4 + finite * d * 4 + Q * H * (d * out_b + 4)
+    merge_bytes = P * Q * H * 4 + finite * d * 4 + Q * H * (d * out_b + 4)
     merge_gbs = merge_bytes / (ph["merge"] * 1e-3) / 1e9
     # credited (useful) FLOP of each main kernel per launch: forward 4d per pair;
     # the backward's 8d per pair (dV, dP, dQ, dK) is credited 6d to the dK/dV
@@ -375,10 +457,8 @@ def run_ours(args):
         h_dq = torch.empty(Q, H, d, dtype=torch.float32, pin_memory=True)
         h_dk = torch.empty(w.S, H, d, dtype=torch.float32, pin_memory=True)
         h_dv = torch.empty(w.S, H, d, dtype=torch.float32, pin_memory=True)
-        h_dkb = torch.empty(Q, H, d, dtype=torch.float32, pin_memory=True)
-        h_dvb = torch.empty(Q, H, d, dtype=torch.float32, pin_memory=True)
-        h_in = [(x.cpu().pin_memory(), x) for x in (s, a, q, k, v, kb, vb, dO)]
-        h_out = [(o, h_o), (lse, h_lse), (dq, h_dq), (dk, h_dk), (dv, h_dv), (dkb, h_dkb), (dvb, h_dvb)]
+        h_in = [(x.cpu().pin_memory(), x) for x in (s, a, q, k, v, dO)]
+        h_out = [(o, h_o), (lse, h_lse), (dq, h_dq), (dk, h_dk), (dv, h_dv)]
         bi = sum(x.numel() * x.element_size() for x, _ in h_in)
         bo = sum(x.numel() * x.element_size() for x, _ in h_out)
 
@@ -408,7 +488,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, desc, _ = oracle_sample(w, inp, kb, vb, args.cpu_budget_s)
+        tf, desc, _ = oracle_sample(w, inp, args.cpu_budget_s)
         cpu = {"value": tf, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc}
 
     if rank == 0:
@@ -419,7 +499,7 @@ def run_ours(args):
             "config": {"workload": w.name, "b": w.n_samples, "S": w.S, "Q": w.Q, "B": w.B, "H": H, "d": d,
                        "m": w.m, "P": P, "J": w.J, "order": w.order,
                        "l2": "inputs larger than L2 (K+V alone exceed 129 MB)",
-                       "mask": "context windows + block-local B x B",
+                       "mask": "context windows (block-local term: block_local object)",
                        "parallelism": f"{world} independent replica(s)"},
             "pct_bf16_peak": {"measured_sustained": value / world / sustained,
                               "nominal_2250": value / world / 2250.0},
@@ -431,6 +511,10 @@ def run_ours(args):
                          "peak": sustained, "unit": "TFLOP/s", "frac": dom_tf / sustained,
                          "peak_kind": f"{pk_kind} sustained bf16", "traffic": traffic},
             "kernels": kernels,
+            "block_local": {"term": "each block's rows over its own B keys (one more merged partial)",
+                            "whole_mask_ms_per_step": whole_ms,
+                            "fwd": kernels.get("block_local_fwd_kernel"),
+                            "bwd": kernels.get("block_local_bwd_kernel")},
             "gpu_launches": int(launches),
             "clocks": clk,
             "e2e": e2e,
@@ -453,7 +537,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=4.0)
+    ap.add_argument("--study", choices=["planners"], default=None,
+                    help="instead of the step benchmark: the planner rho / latency study")
     args = ap.parse_args()
+    if args.study == "planners":
+        return run_planner_study(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
