@@ -166,12 +166,13 @@ SKV_API skv_status skv_attn_fwd(const skv_problem* prob, const void* q, const vo
  * has no counterpart to this call; it is a packaging of skv_attn_fwd.
  *
  * Same arguments, semantics and outputs as skv_attn_fwd.  The scratch the
- * forward needs (the per-rank chunk lists) lives in a fixed 128 KiB array in
- * device memory that every GPU loading the library holds until the process
- * exits; the call itself allocates nothing.  Problems whose forward workspace
- * (skv_workspace_bytes(prob, 0)) exceeds 131072 bytes are rejected with
- * SKV_ERR_WORKSPACE before any launch -- e.g. P <= 1024 ranks with up to
- * 30 000 chunks fit.
+ * forward needs (the per-rank chunk lists, 4 bytes per chunk and per rank, and
+ * the key bounds of each 128-row query tile, 16 bytes each) lives in a fixed
+ * 128 KiB array in device memory that every GPU loading the library holds
+ * until the process exits; the call itself allocates nothing.  Problems whose
+ * forward workspace (skv_workspace_bytes(prob, 0)) exceeds 131072 bytes are
+ * rejected with SKV_ERR_WORKSPACE before any launch -- e.g. 16384 chunks over
+ * 1024 ranks with up to 3800 query tiles (Q <= 486 400 rows) fit.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream

@@ -13,8 +13,8 @@
 
 #include "skv_common.cuh"
 
-// Capacity of the static scratch: 128 KiB (enough for the chunk lists of any
-// plan with P <= 1024 ranks and up to 30 000 chunks).
+// Capacity of the static scratch: 128 KiB (the chunk lists of a plan with 16384
+// chunks over 1024 ranks plus the key bounds of 3800 query tiles fit).
 constexpr size_t kStaticScratchBytes = 131072;
 
 static __device__ __align__(256) unsigned char g_fwd_static_scratch[kStaticScratchBytes];
