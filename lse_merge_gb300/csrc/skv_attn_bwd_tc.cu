@@ -18,10 +18,11 @@
 //  * attn_bwd_dq_tc_kernel -- query-stationary.  One thread block owns a
 //    128-row query tile and a head and walks, rank by rank, the key tiles of
 //    every rank's chunks that meet the tile's windows: dq = sum_p dq^(p)
-//    (Alg. 1 line 17) is accumulated in TMEM and written once.  Per key tile:
-//      S = Q K^T, dP = dO V^T (SS); eight warps form dS (bf16 -> TMEM over S);
-//      dQ += dS K (TS).  dP of the next tile is issued as soon as dP has been
-//      read, ahead of the dQ MMA, so it overlaps the forming of dS.
+//    (Alg. 1 line 17) is accumulated in TMEM and written once.  Q and dO stay
+//    in TMEM as A operands; per key tile:
+//      S = Q K^T, dP = dO V^T (TS); eight warps form dS (bf16 -> TMEM over the
+//      dP they read); dQ += dS K (TS).  S of the next tile is issued as soon as
+//      S has been read, so it overlaps the forming of P and dS.
 // Recomputing S and dP in the second kernel costs two extra GEMMs per tile pair
 // but removes every dq reduction from the key-stationary loop.
 #include <cuda.h>
@@ -494,27 +495,28 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
 }
 
 // =================================================================== dQ
+//
+// Q and dO of the block's query tile stay in TMEM for the whole walk (the
+// compute warps copy them there once, as the bf16 pairs an A operand takes), so
+// all three MMAs read only their B operand from shared memory:
+//   S = Q K_n^T (TS) -> TMEM S;   dP = dO V_n^T (TS) -> TMEM dP;
+//   dS = P (dP - D) as bf16 over the dP columns just read;   dQ += dS K_n (TS).
+// S of the next key tile is issued as soon as S has been read; dP of the next
+// tile follows the dQ MMA that reads dS from the same columns.
 
 constexpr int kQThreads = 320;                       // compute warps 0-7, MMA 8, TMA 9
 constexpr int kQMma = 8, kQTma = 9;
-constexpr int kKStages = 3, kVStages = 2;
+constexpr int kKStages = 4, kVStages = 3;
 
 template <int D>
 struct QTiles {                                      // 1024-byte aligned
-    __nv_bfloat16 q[D / 64][BM * 64];
-    __nv_bfloat16 dO[D / 64][BM * 64];
     __nv_bfloat16 k[kKStages][D / 64][BN * 64];
     __nv_bfloat16 v[kVStages][D / 64][BN * 64];
 };
 
-struct QMeta {
-    float lse2[BM];
-    float D[BM];
-};
-
 struct QBars {
-    uint64_t q_full, k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-    uint64_t s_full[2], dp_full, dp_read, ds_full, mma_fin, stuck;
+    uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+    uint64_t qd_tmem, s_full, s_read, dp_full, ds_full, mma_fin, stuck;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -522,14 +524,13 @@ struct QBars {
 template <int D>
 struct QSmem {
     QTiles<D> t;
-    QMeta meta;
     QBars b;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kQThreads, 1)
-attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
-                      const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                      const __nv_bfloat16* __restrict__ qg, const __nv_bfloat16* __restrict__ dOg,
                       const float* __restrict__ lse2_hm, const float* __restrict__ D_hm, int64_t Qp,
                       const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int64_t Qn, int H,
                       int64_t S, int m, int P, float scale, float scale_log2, const int4* __restrict__ qtb,
@@ -556,7 +557,6 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
     it.init(csr, 0, P, m, bnd.x, bnd.y);             // every rank's chunks: dq = sum_p dq^(p)
 
     if (tid == 0) {
-        mbar_init(&bb.q_full, 1);
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(&bb.k_full[i], 1);
             mbar_init(&bb.k_empty[i], 1);
@@ -565,10 +565,10 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
             mbar_init(&bb.v_full[i], 1);
             mbar_init(&bb.v_empty[i], 1);
         }
-        mbar_init(&bb.s_full[0], 1);
-        mbar_init(&bb.s_full[1], 1);
+        mbar_init(&bb.qd_tmem, 256);
+        mbar_init(&bb.s_full, 1);
+        mbar_init(&bb.s_read, 256);
         mbar_init(&bb.dp_full, 1);
-        mbar_init(&bb.dp_read, 256);
         mbar_init(&bb.ds_full, 256);
         mbar_init(&bb.mma_fin, 1);
         mbar_init(&bb.stuck, 1);
@@ -583,34 +583,28 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bb.tmem_base;
-    const uint32_t tS = tmem, tP = tmem + 256, tQ = tmem + 384;   // S double buffer, dP, dQ accumulator
+    // S, dP (dS bf16 over it), dQ accumulator, Q and dO as bf16 A operands
+    const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256, tQin = tmem + 384, tDO = tmem + 448;
     auto abort_now = [&]() {
         atomicExch(&bb.abort_flag, 1);
         skv::raise_status(status, SKV_ERR_TIMEOUT);
     };
 
     if (warp == kQTma) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ TMA producer: K and V rings
         if (lane == 0) {
             int n = 0;       // key tiles whose K load was issued
             int nv = 0;      // key tiles whose V load was issued
             int64_t x0, xa;
-            bool any = false;
             // K/V of the tile two ahead go to L2 while this one loads
             TileIter ahead = it;
             for (int i = 0; i < 2; ++i) ahead.next(xa);
+            bool first = true;
             while (it.next(x0)) {
-                if (!any) {
+                if (first) {
                     prefetch_tensormap(&map_k);
                     prefetch_tensormap(&map_v);
-                    mbar_arrive_expect_tx(&bb.q_full, 2 * kTile + 2 * BM * 4);
-                    for (int c = 0; c < NP; ++c) {
-                        tma_load_2d(tl.q[c], &map_q, &bb.q_full, h * D + c * 64, qt * BM);
-                        tma_load_2d(tl.dO[c], &map_do, &bb.q_full, h * D + c * 64, qt * BM);
-                    }
-                    bulk_load(sm.meta.lse2, lse2_hm + int64_t(h) * Qp + int64_t(qt) * BM, BM * 4, &bb.q_full);
-                    bulk_load(sm.meta.D, D_hm + int64_t(h) * Qp + int64_t(qt) * BM, BM * 4, &bb.q_full);
-                    any = true;
+                    first = false;
                 }
                 const int ks = n % kKStages, vs = n % kVStages;
                 if (n >= kKStages &&
@@ -637,7 +631,6 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
                 ++nv;
             }
             // every copy issued has landed before the block exits
-            if (any) mbar_wait(&bb.q_full, 0, kTeardownWait);
             for (int st = 0; st < kKStages && st < n; ++st) {
                 const int last = st + ((n - 1 - st) / kKStages) * kKStages;
                 mbar_wait(&bb.k_full[st], (last / kKStages) & 1, kTeardownWait);
@@ -660,13 +653,12 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
         bool issued = false;
         bool ok = T > 0;
         if (ok && stuck_test && !wait(&bb.stuck, 0)) ok = false;
-        if (ok) ok = wait(&bb.q_full, 0);
+        if (ok) ok = wait(&bb.qd_tmem, 0);
         // shared-memory descriptors as offsets (bytes / 16) from the first panel
         constexpr uint32_t kPanel = BN * 64 * 2 / 16, kSt = NP * kPanel;
-        const uint64_t dQ = smem_desc(smem_u32(tl.q[0]), 16, 1024), dDO = smem_desc(smem_u32(tl.dO[0]), 16, 1024);
         const uint64_t dK = smem_desc(smem_u32(tl.k[0][0]), 16, 1024), dV = smem_desc(smem_u32(tl.v[0][0]), 16, 1024);
         const uint64_t dKmn = smem_desc(smem_u32(tl.k[0][0]), BN * 128, 1024);
-        auto issue_s = [&](int n) -> bool {            // S_n = Q K_n^T -> S[n&1]
+        auto issue_s = [&](int n) -> bool {            // S_n = Q K_n^T -> S
             const int ks = n % kKStages;
             if (!wait(&bb.k_full[ks], (n / kKStages) & 1)) return false;
             tc_fence_after();
@@ -674,9 +666,9 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
-                    mma_ss(tS + (n & 1) * 128, dQ + off, dK + (ks * kSt + off), idS, kk > 0);
+                    mma_ts(tS, tQin + kk * 8, dK + (ks * kSt + off), idS, kk > 0);
                 }
-                mma_commit(&bb.s_full[n & 1]);
+                mma_commit(&bb.s_full);
             }
             __syncwarp();
             issued = true;
@@ -690,7 +682,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
-                    mma_ss(tP, dDO + off, dV + (vs * kSt + off), idS, kk > 0);
+                    mma_ts(tP, tDO + kk * 8, dV + (vs * kSt + off), idS, kk > 0);
                 }
                 mma_commit(&bb.dp_full);
                 mma_commit(&bb.v_empty[vs]);
@@ -699,30 +691,29 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
             issued = true;
             return true;
         };
-        if (ok) ok = issue_s(0) && issue_dp(0) && (T < 2 || issue_s(1));
+        if (ok) ok = issue_s(0) && issue_dp(0);
         for (int n = 0; ok && n < T; ++n) {
-            // dP_{n+1} overwrites dP as soon as the compute warps have read dP_n,
-            // ahead of the dQ MMA that waits for dS_n
+            // S_{n+1} overwrites S as soon as the compute warps have read S_n
             if (n + 1 < T) {
-                if (!wait(&bb.dp_read, n & 1)) { ok = false; break; }
+                if (!wait(&bb.s_read, n & 1)) { ok = false; break; }
                 tc_fence_after();
-                if (!issue_dp(n + 1)) { ok = false; break; }
+                if (!issue_s(n + 1)) { ok = false; break; }
             }
             if (!wait(&bb.ds_full, n & 1)) { ok = false; break; }
             tc_fence_after();
             // dQ += dS_n K_n: bf16 dS of key columns [64h, 64h+64) sits in TMEM columns
-            // [64h, 64h+32) of S[n&1]
+            // [64h, 64h+32) of dP
             const int ks = n % kKStages;
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tQ, tS + (n & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8, dKmn + (ks * kSt + kk * 128),
-                           idQ, (n > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tQ, tP + (kk >> 2) * 64 + (kk & 3) * 8, dKmn + (ks * kSt + kk * 128), idQ,
+                           (n > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bb.k_empty[ks]);
             }
             __syncwarp();
-            // S_{n+2} overwrites S[n&1] right behind the dQ MMA that reads dS_n from it
-            if (n + 2 < T && !issue_s(n + 2)) { ok = false; break; }
+            // dP_{n+1} overwrites dP right behind the dQ MMA that reads dS_n from it
+            if (n + 1 < T && !issue_dp(n + 1)) { ok = false; break; }
         }
         if (!ok && T > 0 && lane == 0) abort_now();
         if (issued) {
@@ -749,24 +740,42 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
             if (!got && lane == 0) abort_now();
             return got;
         };
-        float l2 = INFINITY, Dr = 0.f;
+        {   // this row of Q (warps of half 0) or dO (half 1) into TMEM as bf16 pairs
+            const __nv_bfloat16* src = (hf == 0 ? qg : dOg) + (row * H + h) * D;
+            const uint32_t dst = (hf == 0 ? tQin : tDO) + lane_base;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t w[32];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    uint4 v4 = make_uint4(0u, 0u, 0u, 0u);
+                    if (live) v4 = *reinterpret_cast<const uint4*>(src + c * 64 + u * 8);
+                    w[4 * u] = v4.x;
+                    w[4 * u + 1] = v4.y;
+                    w[4 * u + 2] = v4.z;
+                    w[4 * u + 3] = v4.w;
+                }
+                tmem_st32(dst + c * 32, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bb.qd_tmem);
+        }
+        const float l2 = live ? lse2_hm[int64_t(h) * Qp + row] : INFINITY;
+        const float Dr = live ? D_hm[int64_t(h) * Qp + row] : 0.f;
         int64_t x0;
         int n = 0;
         while (it.next(x0)) {
-            if (n == 0) {
-                if (!uniform_wait(&bb.q_full, 0)) { ok = false; break; }
-                l2 = sm.meta.lse2[r];
-                Dr = sm.meta.D[r];
-            }
             if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
             const bool full = (x0 >= bnd.z) && (x0 + BN <= bnd.w);
-            const uint32_t sbuf = tS + (n & 1) * 128;
-            if (!uniform_wait(&bb.s_full[n & 1], (n >> 1) & 1)) { ok = false; break; }
+            if (!uniform_wait(&bb.s_full, n & 1)) { ok = false; break; }
             tc_fence_after();
             uint32_t sraw[2][32];
-            tmem_ld32(sbuf + lane_base + hf * 64, sraw[0]);
-            tmem_ld32(sbuf + lane_base + hf * 64 + 32, sraw[1]);
+            tmem_ld32(tS + lane_base + hf * 64, sraw[0]);
+            tmem_ld32(tS + lane_base + hf * 64 + 32, sraw[1]);
             tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&bb.s_read);                     // S is free for the next tile
             float pr[2][32];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -801,8 +810,6 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
             tmem_ld32(tP + lane_base + hf * 64, draw[0]);
             tmem_ld32(tP + lane_base + hf * 64 + 32, draw[1]);
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&bb.dp_read);                    // dP is free for the next tile
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t pk[16];
@@ -811,12 +818,12 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_co
                 for (int j = 0; j < 16; ++j) {
                     const float2 t = __fadd2_rn(
                         make_float2(__uint_as_float(draw[c][2 * j]), __uint_as_float(draw[c][2 * j + 1])), nd2);
-                    const float2 d = __fmul2_rn(make_float2(pr[c][2 * j], pr[c][2 * j + 1]), t);
-                    pk[j] = pack_bf16(d.x, d.y);
+                    const float2 dd = __fmul2_rn(make_float2(pr[c][2 * j], pr[c][2 * j + 1]), t);
+                    pk[j] = pack_bf16(dd.x, dd.y);
                 }
                 // bf16 dS of key columns [64hf + 32c, +32) -> TMEM columns [64hf + 16c, +16)
-                // of this S buffer: inside this warp's half, over columns read already
-                tmem_st16(sbuf + lane_base + hf * 64 + c * 16, pk);
+                // of dP: inside this warp's half, over columns read already
+                tmem_st16(tP + lane_base + hf * 64 + c * 16, pk);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -915,8 +922,9 @@ skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const
         SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax));
         skv_host::timer_begin(skv_host::kTimeBwdQ, c.stream);
         kern<<<dim3((unsigned)n_qt, (unsigned)pb.n_heads), kQThreads, kSmemMax, c.stream>>>(
-            mq, mdo, mk, mv, lse2_hm, D_hm, Qp, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.m, pb.P, pb.scale,
-            scale_log2, w.qtb, csr, dq, c.status, c.wait_limit);
+            mk, mv, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), lse2_hm, D_hm, Qp,
+            pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.m, pb.P, pb.scale, scale_log2, w.qtb, csr, dq, c.status,
+            c.wait_limit);
         skv_host::timer_end(skv_host::kTimeBwdQ, c.stream);
         SKV_LAUNCHED();
     }
