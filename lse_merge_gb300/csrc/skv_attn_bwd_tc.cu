@@ -11,10 +11,11 @@
 //    tile-skip list (built by qtile_bounds_kernel / kv_list_kernel; masked-out
 //    query tiles are never loaded).  Per query tile t:
 //      S^T = K Q_t^T, dP^T = V dO_t^T (SS) -> TMEM A, B
-//      eight warps: P^T = exp2(S^T scale log2e - l2), dS^T = P^T (dP^T - D),
-//                   both bf16 -> TMEM B over the dP^T they have read
-//      dV += P^T dO_t, dK += dS^T Q_t (TS: A operands from TMEM); S of the next
-//      tile is issued as soon as S^T has been read, so it overlaps the exponentials
+//      eight warps: P^T = exp2(S^T scale log2e - l2) as bf16 -> TMEM A over the
+//                   S^T they have read; dS^T = P^T (dP^T - D) -> TMEM B likewise
+//      dV += P^T dO_t (TS) as soon as P^T is in TMEM, so it overlaps the forming
+//      of dS^T; then S of the next tile; dK += dS^T Q_t (TS); dP of the next tile.
+//    dK and dV leave through shared memory with TMA stores.
 //  * attn_bwd_dq_tc_kernel -- query-stationary.  One thread block owns a
 //    128-row query tile and a head and walks, rank by rank, the key tiles of
 //    every rank's chunks that meet the tile's windows: dq = sum_p dq^(p)
@@ -104,7 +105,7 @@ struct KvMeta {                                      // per query tile, loaded w
 };
 
 struct KvBars {
-    uint64_t kv_full, q_full[2], q_empty[2], do_full[2], do_empty[2], s_full, s_read, dp_full, ds_full, mma_fin;
+    uint64_t kv_full, q_full[2], q_empty[2], do_full[2], do_empty[2], s_full, p_full, dp_full, ds_full, mma_fin;
     uint64_t stuck;                                  // never completed: target of the forced-timeout test mode
     uint32_t tmem_base;
     int abort_flag;
@@ -121,6 +122,7 @@ template <int D>
 __global__ void __launch_bounds__(kKvThreads, 1)
 attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                         const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                        const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
                         const float* __restrict__ lse2_hm, const float* __restrict__ D_hm, int64_t Qp,
                         const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int64_t Qn, int H,
                         int64_t S, float scale, float scale_log2, const int4* __restrict__ qtb,
@@ -159,7 +161,7 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             mbar_init(&bb.do_empty[i], 1);
         }
         mbar_init(&bb.s_full, 1);
-        mbar_init(&bb.s_read, 256);
+        mbar_init(&bb.p_full, 256);
         mbar_init(&bb.dp_full, 1);
         mbar_init(&bb.ds_full, 256);
         mbar_init(&bb.mma_fin, 1);
@@ -289,14 +291,25 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 tc_fence_after();
                 issue_dp(0);
             }
-            // per query tile t:
-            //   [S_t read]  S_{t+1} -> A   (overlaps the compute warps' P_t / dS_t)
-            //   [dS_t done] dK_t += dS_t Q_t, dV_t += P_t dO_t (P_t, dS_t bf16 in B over the
-            //               read dP_t), then dP_{t+1} -> B behind them in issue order
+            // per query tile t (in issue order):
+            //   [P_t stored]  dV += P_t^T dO_t   (P_t bf16 over the read S_t), while dS_t forms
+            //   S_{t+1} -> A  right behind the dV MMAs reading P_t from A
+            //   [dS_t stored] dK += dS_t^T Q_t   (dS_t bf16 over the read dP_t)
+            //   dP_{t+1} -> B right behind the dK MMAs reading dS_t from B
             for (int t = 0; ok && t < cnt; ++t) {
                 const int st = t & 1;
                 const bool more = t + 1 < cnt;
-                if (!wait(&bb.s_read, t & 1)) { ok = false; break; }
+                if (!wait(&bb.p_full, t & 1)) { ok = false; break; }
+                tc_fence_after();
+                // bf16 P^T of query columns [64h, 64h+64) sits in TMEM columns [64h, 64h+32) of A
+                if (elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < BM / 16; ++kk)
+                        mma_ts(tdV, tA + (kk >> 2) * 64 + (kk & 3) * 8, dDOmn + (st * kSt + kk * 128), idKV,
+                               (t > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bb.do_empty[st]);
+                }
+                __syncwarp();
                 if (more) {
                     if (!wait(&bb.q_full[(t + 1) & 1], ((t + 1) >> 1) & 1)) { ok = false; break; }
                     tc_fence_after();
@@ -304,23 +317,15 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 }
                 if (!wait(&bb.ds_full, t & 1)) { ok = false; break; }
                 tc_fence_after();
-                // dK += dS^T Q.  bf16 P^T of query columns [64h, 64h+64) sits in TMEM columns
-                // [64h, 64h+32) of B and dS^T in [64h+32, 64h+64) (each half of the compute
-                // warps writes inside its half)
+                // bf16 dS^T of query columns [64h, 64h+64) sits in TMEM columns [64h, 64h+32) of B
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < BM / 16; ++kk)
-                        mma_ts(tdK, tB + (kk >> 2) * 64 + 32 + (kk & 3) * 8, dQmn + (st * kSt + kk * 128), idKV,
+                        mma_ts(tdK, tB + (kk >> 2) * 64 + (kk & 3) * 8, dQmn + (st * kSt + kk * 128), idKV,
                                (t > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(&bb.q_empty[st]);
-#pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk)  // dV += P^T dO
-                        mma_ts(tdV, tB + (kk >> 2) * 64 + (kk & 3) * 8, dDOmn + (st * kSt + kk * 128), idKV,
-                               (t > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bb.do_empty[st]);
                 }
                 __syncwarp();
-                // dP_{t+1} overwrites B right behind the dK and dV MMAs reading dS_t, P_t from it
                 if (more) {
                     if (!wait(&bb.do_full[(t + 1) & 1], ((t + 1) >> 1) & 1)) { ok = false; break; }
                     tc_fence_after();
@@ -360,15 +365,12 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             const bool full = (x0 >= bnd.z) && (x0 + BN <= bnd.w);
             if (!uniform_wait(&bb.s_full, t & 1)) { ok = false; break; }
             tc_fence_after();
-            // both 32-column chunks of S^T are loaded before one wait; A is then free
-            // for S of the next tile.  P^T is kept as the bf16 pairs the dV MMA
-            // consumes and dS^T is formed from those values.
+            // both 32-column chunks of S^T are loaded before one wait.  P^T is kept as
+            // the bf16 pairs the dV MMA consumes and dS^T is formed from those values.
             uint32_t sraw[2][32];
             tmem_ld32(tA + lane_base + hf * 64, sraw[0]);
             tmem_ld32(tA + lane_base + hf * 64 + 32, sraw[1]);
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&bb.s_read);
             uint32_t pk[2][16];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -416,16 +418,19 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                     }
                 }
             }
+            // bf16 P^T of columns [64hf + 32c, +32) -> TMEM A columns [64hf + 16c, +16):
+            // inside this warp's half, over S^T columns it has just read
+            tmem_st16(tA + lane_base + hf * 64, pk[0]);
+            tmem_st16(tA + lane_base + hf * 64 + 16, pk[1]);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bb.p_full);
             if (!uniform_wait(&bb.dp_full, t & 1)) { ok = false; break; }
             tc_fence_after();
             uint32_t draw[2][32];
             tmem_ld32(tB + lane_base + hf * 64, draw[0]);
             tmem_ld32(tB + lane_base + hf * 64 + 32, draw[1]);
             tmem_ld_wait();
-            // bf16 P^T of columns [64hf + 32c, +32) -> TMEM B columns [64hf + 16c, +16):
-            // inside this warp's half, over dP^T columns it has just read
-            tmem_st16(tB + lane_base + hf * 64, pk[0]);
-            tmem_st16(tB + lane_base + hf * 64 + 16, pk[1]);
             uint32_t d2[2][16];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -446,38 +451,61 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                     d2[c][2 * j4 + 1] = pack_bf16(d23.x, d23.y);
                 }
             }
-            // bf16 dS^T of columns [64hf + 32c, +32) -> TMEM B columns [64hf + 32 + 16c, +16)
-            tmem_st16(tB + lane_base + hf * 64 + 32, d2[0]);
-            tmem_st16(tB + lane_base + hf * 64 + 48, d2[1]);
+            // bf16 dS^T of columns [64hf + 32c, +32) -> TMEM B columns [64hf + 16c, +16)
+            tmem_st16(tB + lane_base + hf * 64, d2[0]);
+            tmem_st16(tB + lane_base + hf * 64 + 16, d2[1]);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bb.ds_full);
         }
-        // dK (scaled) and dV rows of this key tile, columns split between the two
-        // halves, once every MMA of the block has completed; zeros if no query sees it
+        // dK (scaled) and dV rows of this key tile, once every MMA of the block has
+        // completed; zeros if no query sees it.  Each warp stages its 32 rows x D/2
+        // columns in the (now idle) Q and dO rings as 128-byte-swizzled 32x32 fp32
+        // boxes and writes them with TMA stores (rows past S are dropped).
         const bool aborted = __any_sync(kAll, *(volatile int*)&bb.abort_flag != 0);
         constexpr int kHalf = D / 2;
-        float* dkr = dk + (x * H + h) * D + hf * kHalf;
-        float* dvr = dv + (x * H + h) * D + hf * kHalf;
         if (cnt > 0 && ok && !aborted && uniform_wait(&bb.mma_fin, 0)) {
             tc_fence_after();
+            unsigned char* stage_k = reinterpret_cast<unsigned char*>(&tl.q[0][0][0]);
+            unsigned char* stage_v = reinterpret_cast<unsigned char*>(&tl.dO[0][0][0]);
+            const uint32_t row_off = uint32_t(r) * 128u;
 #pragma unroll
             for (int c = 0; c < kHalf / 32; ++c) {
                 uint32_t rk[32], rv[32];
                 tmem_ld32(tdK + lane_base + hf * kHalf + c * 32, rk);
                 tmem_ld32(tdV + lane_base + hf * kHalf + c * 32, rv);
                 tmem_ld_wait();
+                // panel of columns [32p, 32p+32): 128 rows x 128 bytes; 16-byte chunk j of
+                // row r sits at chunk j ^ (r % 8)
+                const uint32_t panel = uint32_t(hf * (kHalf / 32) + c) * (BN * 128u);
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    __stcs(reinterpret_cast<float4*>(dkr + c * 32 + j),
-                           make_float4(scale * __uint_as_float(rk[j]), scale * __uint_as_float(rk[j + 1]),
-                                       scale * __uint_as_float(rk[j + 2]), scale * __uint_as_float(rk[j + 3])));
-                    __stcs(reinterpret_cast<float4*>(dvr + c * 32 + j),
-                           make_float4(__uint_as_float(rv[j]), __uint_as_float(rv[j + 1]), __uint_as_float(rv[j + 2]),
-                                       __uint_as_float(rv[j + 3])));
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t off = panel + row_off + uint32_t((j ^ (r & 7)) * 16);
+                    *reinterpret_cast<float4*>(stage_k + off) =
+                        make_float4(scale * __uint_as_float(rk[4 * j]), scale * __uint_as_float(rk[4 * j + 1]),
+                                    scale * __uint_as_float(rk[4 * j + 2]), scale * __uint_as_float(rk[4 * j + 3]));
+                    *reinterpret_cast<float4*>(stage_v + off) =
+                        make_float4(__uint_as_float(rv[4 * j]), __uint_as_float(rv[4 * j + 1]),
+                                    __uint_as_float(rv[4 * j + 2]), __uint_as_float(rv[4 * j + 3]));
                 }
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+                for (int c = 0; c < kHalf / 32; ++c) {
+                    const int p = hf * (kHalf / 32) + c;
+                    const uint32_t off = uint32_t(p) * (BN * 128u) + uint32_t(quad * 32) * 128u;
+                    tma_store_2d(&map_dk, stage_k + off, h * D + p * 32, (int)(x0 + quad * 32));
+                    tma_store_2d(&map_dv, stage_v + off, h * D + p * 32, (int)(x0 + quad * 32));
+                }
+                bulk_commit_group();
+                bulk_wait_read_all();
+            }
+            __syncwarp();
         } else if (cnt == 0) {
+            float* dkr = dk + (x * H + h) * D + hf * kHalf;
+            float* dvr = dv + (x * H + h) * D + hf * kHalf;
             const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < kHalf; j += 4) {
@@ -901,10 +929,10 @@ skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const
     SKV_LAUNCHED();
     kv_list_kernel<<<(n_kv + 7) / 8, 256, 0, c.stream>>>(w.qtb, n_qt, n_kv, w.cnt, w.list);
     SKV_LAUNCHED();
-    CUtensorMap mq, mdo, mk, mv;
+    CUtensorMap mq, mdo, mk, mv, mdk, mdv;
     const int64_t cols = int64_t(pb.n_heads) * D;
     if (!make_map(&mq, q, Qn, cols) || !make_map(&mdo, dO, Qn, cols) || !make_map(&mk, k, pb.S, cols) ||
-        !make_map(&mv, v, pb.S, cols))
+        !make_map(&mv, v, pb.S, cols) || !make_map_f32(&mdk, dk, pb.S, cols) || !make_map_f32(&mdv, dv, pb.S, cols))
         return SKV_ERR_CUDA;
     const float scale_log2 = pb.scale * 1.4426950408889634f;
     {
@@ -912,7 +940,7 @@ skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const
         SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax));
         skv_host::timer_begin(skv_host::kTimeBwdKV, c.stream);
         kern<<<dim3((unsigned)n_kv, (unsigned)pb.n_heads), kKvThreads, kSmemMax, c.stream>>>(
-            mq, mdo, mk, mv, lse2_hm, D_hm, Qp, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.scale, scale_log2, w.qtb,
+            mq, mdo, mk, mv, mdk, mdv, lse2_hm, D_hm, Qp, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.scale, scale_log2, w.qtb,
             w.cnt, w.list, n_qt, dk, dv, c.status, c.wait_limit);
         skv_host::timer_end(skv_host::kTimeBwdKV, c.stream);
         SKV_LAUNCHED();
