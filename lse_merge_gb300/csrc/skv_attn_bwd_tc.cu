@@ -88,15 +88,17 @@ __global__ void kv_list_kernel(const int4* __restrict__ qtb, int n_qt, int n_kv,
 constexpr int kKvThreads = 320;                      // compute warps 0-7, MMA 8, TMA 9
 constexpr int kKvMma = 8, kKvTma = 9;
 
+constexpr int kQSt = 3;                              // Q ring depth (dO and metadata: 2)
+
 template <int D>
 struct KvTiles {                                     // 1024-byte aligned (128-byte swizzle atoms)
     __nv_bfloat16 k[D / 64][BN * 64];
     __nv_bfloat16 v[D / 64][BN * 64];
-    __nv_bfloat16 q[2][D / 64][BM * 64];
+    __nv_bfloat16 q[kQSt][D / 64][BM * 64];
     __nv_bfloat16 dO[2][D / 64][BM * 64];
 };
 
-struct KvMeta {                                      // per query tile, loaded with its Q/dO stage
+struct KvMeta {                                      // per query tile, its own two-stage ring
     float lse2[BM];
     float D[BM];
     int4 bnd;                                        // the tile's key bounds (written by the producer)
@@ -105,7 +107,8 @@ struct KvMeta {                                      // per query tile, loaded w
 };
 
 struct KvBars {
-    uint64_t kv_full, q_full[2], q_empty[2], do_full[2], do_empty[2], s_full, p_full, dp_full, ds_full, mma_fin;
+    uint64_t kv_full, q_full[kQSt], q_empty[kQSt], meta_full[2], meta_empty[2], do_full[2], do_empty[2];
+    uint64_t s_full, p_full[2], dp_full, ds_full, mma_fin;
     uint64_t stuck;                                  // never completed: target of the forced-timeout test mode
     uint32_t tmem_base;
     int abort_flag;
@@ -154,14 +157,19 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
 
     if (tid == 0) {
         mbar_init(&bb.kv_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kQSt; ++i) {
             mbar_init(&bb.q_full[i], 1);
             mbar_init(&bb.q_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bb.meta_full[i], 1);
+            mbar_init(&bb.meta_empty[i], 256);
             mbar_init(&bb.do_full[i], 1);
             mbar_init(&bb.do_empty[i], 1);
         }
         mbar_init(&bb.s_full, 1);
-        mbar_init(&bb.p_full, 256);
+        mbar_init(&bb.p_full[0], 256);
+        mbar_init(&bb.p_full[1], 256);
         mbar_init(&bb.dp_full, 1);
         mbar_init(&bb.ds_full, 256);
         mbar_init(&bb.mma_fin, 1);
@@ -193,25 +201,33 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 tma_load_2d(tl.k[c], &map_k, &bb.kv_full, h * D + c * 64, (int)x0);
                 tma_load_2d(tl.v[c], &map_v, &bb.kv_full, h * D + c * 64, (int)x0);
             }
-            // Q (with the tile's metadata) and dO have their own rings: the dK MMA frees
-            // Q before the dV MMA frees dO, and S of a tile needs Q before dP needs dO
-            int nq = 0, nd = 0;
+            // Q, the tile's metadata (l2, D, bounds) and dO have their own rings: the dK
+            // MMA frees Q, the compute warps free the metadata once dS is formed and the
+            // dV MMA frees dO; S of a tile needs Q first, so Q runs one stage deeper
+            int nq = 0, nm = 0, nd = 0;
             for (int t = 0; t < cnt; ++t) {
-                const int st = t & 1;
-                if (t >= 2 && !mbar_wait(&bb.q_empty[st], ((t - 2) >> 1) & 1, wait_limit, &bb.abort_flag)) {
+                const int sq = t % kQSt, st = t & 1;
+                if (t >= kQSt &&
+                    !mbar_wait(&bb.q_empty[sq], ((t - kQSt) / kQSt) & 1, wait_limit, &bb.abort_flag)) {
                     abort_now();
                     break;
                 }
                 if (*(volatile int*)&bb.abort_flag) break;
                 const int qt = list[t];
                 const int row = qt * BM;
+                mbar_arrive_expect_tx(&bb.q_full[sq], kTile);
+                for (int c = 0; c < NP; ++c) tma_load_2d(tl.q[sq][c], &map_q, &bb.q_full[sq], h * D + c * 64, row);
+                ++nq;
+                if (t >= 2 && !mbar_wait(&bb.meta_empty[st], ((t - 2) >> 1) & 1, wait_limit, &bb.abort_flag)) {
+                    abort_now();
+                    break;
+                }
                 sm.meta[st].qt = qt;                     // made visible by the arrive below
                 sm.meta[st].bnd = qtb[qt];
-                mbar_arrive_expect_tx(&bb.q_full[st], kTile + 2 * BM * 4);
-                for (int c = 0; c < NP; ++c) tma_load_2d(tl.q[st][c], &map_q, &bb.q_full[st], h * D + c * 64, row);
-                bulk_load(sm.meta[st].lse2, lse2_hm + int64_t(h) * Qp + row, BM * 4, &bb.q_full[st]);
-                bulk_load(sm.meta[st].D, D_hm + int64_t(h) * Qp + row, BM * 4, &bb.q_full[st]);
-                ++nq;
+                mbar_arrive_expect_tx(&bb.meta_full[st], 2 * BM * 4);
+                bulk_load(sm.meta[st].lse2, lse2_hm + int64_t(h) * Qp + row, BM * 4, &bb.meta_full[st]);
+                bulk_load(sm.meta[st].D, D_hm + int64_t(h) * Qp + row, BM * 4, &bb.meta_full[st]);
+                ++nm;
                 if (t >= 2 && !mbar_wait(&bb.do_empty[st], ((t - 2) >> 1) & 1, wait_limit, &bb.abort_flag)) {
                     abort_now();
                     break;
@@ -233,10 +249,15 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             }
             // every copy issued has landed before the block exits
             mbar_wait(&bb.kv_full, 0, kTeardownWait);
-            for (int st = 0; st < 2; ++st) {
-                if (st < nq) mbar_wait(&bb.q_full[st], (((nq - 1 - st) >> 1) * 2 + st) >> 1 & 1, kTeardownWait);
-                if (st < nd) mbar_wait(&bb.do_full[st], (((nd - 1 - st) >> 1) * 2 + st) >> 1 & 1, kTeardownWait);
-            }
+            auto drain = [&](uint64_t* bars, int n, int depth) {
+                for (int st = 0; st < depth && st < n; ++st) {
+                    const int last = st + ((n - 1 - st) / depth) * depth;
+                    mbar_wait(&bars[st], (last / depth) & 1, kTeardownWait);
+                }
+            };
+            drain(bb.q_full, nq, kQSt);
+            drain(bb.meta_full, nm, 2);
+            drain(bb.do_full, nd, 2);
         }
     } else if (warp == kKvMma) {
         // ------------------------------------------------------------ MMA issuer
@@ -297,23 +318,32 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             //   [dS_t stored] dK += dS_t^T Q_t   (dS_t bf16 over the read dP_t)
             //   dP_{t+1} -> B right behind the dK MMAs reading dS_t from B
             for (int t = 0; ok && t < cnt; ++t) {
-                const int st = t & 1;
+                const int st = t & 1, sq = t % kQSt, sq1 = (t + 1) % kQSt;
                 const bool more = t + 1 < cnt;
-                if (!wait(&bb.p_full, t & 1)) { ok = false; break; }
-                tc_fence_after();
-                // bf16 P^T of query columns [64h, 64h+64) sits in TMEM columns [64h, 64h+32) of A
-                if (elect_one()) {
+                // bf16 P^T of query columns [64h, 64h+64) sits in TMEM columns [64h, 64h+32) of
+                // A; it arrives in two parts (query columns [64h, 64h+32), then [64h+32, 64h+64)
+                // of both halves), and the dV MMAs of each part go as soon as it is stored
+                bool got = true;
 #pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk)
-                        mma_ts(tdV, tA + (kk >> 2) * 64 + (kk & 3) * 8, dDOmn + (st * kSt + kk * 128), idKV,
-                               (t > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bb.do_empty[st]);
-                }
-                __syncwarp();
-                if (more) {
-                    if (!wait(&bb.q_full[(t + 1) & 1], ((t + 1) >> 1) & 1)) { ok = false; break; }
+                for (int c = 0; c < 2; ++c) {
+                    if (!wait(&bb.p_full[c], t & 1)) { got = false; break; }
                     tc_fence_after();
-                    issue_s((t + 1) & 1);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int kk = (i >> 1) * 4 + c * 2 + (i & 1);
+                            mma_ts(tdV, tA + (kk >> 2) * 64 + (kk & 3) * 8, dDOmn + (st * kSt + kk * 128), idKV,
+                                   (t > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        if (c == 1) mma_commit(&bb.do_empty[st]);
+                    }
+                    __syncwarp();
+                }
+                if (!got) { ok = false; break; }
+                if (more) {
+                    if (!wait(&bb.q_full[sq1], ((t + 1) / kQSt) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_s(sq1);
                 }
                 if (!wait(&bb.ds_full, t & 1)) { ok = false; break; }
                 tc_fence_after();
@@ -321,9 +351,9 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < BM / 16; ++kk)
-                        mma_ts(tdK, tB + (kk >> 2) * 64 + (kk & 3) * 8, dQmn + (st * kSt + kk * 128), idKV,
+                        mma_ts(tdK, tB + (kk >> 2) * 64 + (kk & 3) * 8, dQmn + (sq * kSt + kk * 128), idKV,
                                (t > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bb.q_empty[st]);
+                    mma_commit(&bb.q_empty[sq]);
                 }
                 __syncwarp();
                 if (more) {
@@ -358,7 +388,7 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
         for (int t = 0; t < cnt; ++t) {
             const int st = t & 1;
             if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
-            if (!uniform_wait(&bb.q_full[st], (t >> 1) & 1)) { ok = false; break; }
+            if (!uniform_wait(&bb.meta_full[st], (t >> 1) & 1)) { ok = false; break; }
             const KvMeta& md = sm.meta[st];
             const int64_t row0 = int64_t(md.qt) * BM;
             const int4 bnd = md.bnd;
@@ -376,14 +406,21 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             for (int c = 0; c < 2; ++c) {
                 const int col0 = hf * 64 + c * 32;
                 uint32_t keep = 0xffffffffu;              // columns whose query row sees key x
-                if (!full) {                              // boundary tile: each query row's own window
+                if (!full) {                              // boundary tile: each block's own window
                     keep = 0u;
+                    const int64_t qr0 = row0 + col0;      // query rows [qr0, qr0 + 32) of this chunk
+                    const int64_t qr1 = (qr0 + 32 < Qn ? qr0 + 32 : Qn);
+                    if (qr0 < qr1) {
 #pragma unroll 1
-                    for (int j = 0; j < 32; ++j) {
-                        const int64_t qr = row0 + col0 + j;
-                        int64_t lo = 0, hi = 0;
-                        if (qr < Qn) skv::block_window(s, a, (int)(qr / B), S, lo, hi);
-                        if (lo <= x && x < hi) keep |= 1u << j;
+                        for (int64_t blk = qr0 / B; blk * B < qr1; ++blk) {
+                            int64_t lo, hi;
+                            skv::block_window(s, a, (int)blk, S, lo, hi);
+                            if (lo <= x && x < hi) {
+                                const int64_t j0 = blk * B - qr0, j1 = (blk + 1) * B - qr0;
+                                const int b0 = j0 > 0 ? (int)j0 : 0, b1 = j1 < (qr1 - qr0) ? (int)j1 : (int)(qr1 - qr0);
+                                keep |= (b1 >= 32 ? 0xffffffffu : ((1u << b1) - 1u)) & ~((1u << b0) - 1u);
+                            }
+                        }
                     }
                 }
                 const float4* l4 = reinterpret_cast<const float4*>(md.lse2 + col0);
@@ -417,14 +454,13 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                         pk[c][2 * j4 + 1] = pack_bf16(pv[2], pv[3]);
                     }
                 }
+                // bf16 P^T of columns [64hf + 32c, +32) -> TMEM A columns [64hf + 16c, +16):
+                // inside this warp's half, over S^T columns it has just read
+                tmem_st16(tA + lane_base + hf * 64 + c * 16, pk[c]);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bb.p_full[c]);
             }
-            // bf16 P^T of columns [64hf + 32c, +32) -> TMEM A columns [64hf + 16c, +16):
-            // inside this warp's half, over S^T columns it has just read
-            tmem_st16(tA + lane_base + hf * 64, pk[0]);
-            tmem_st16(tA + lane_base + hf * 64 + 16, pk[1]);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&bb.p_full);
             if (!uniform_wait(&bb.dp_full, t & 1)) { ok = false; break; }
             tc_fence_after();
             uint32_t draw[2][32];
@@ -457,6 +493,7 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bb.ds_full);
+            mbar_arrive(&bb.meta_empty[st]);             // l2, D and the bounds of this tile are read
         }
         // dK (scaled) and dV rows of this key tile, once every MMA of the block has
         // completed; zeros if no query sees it.  Each warp stages its 32 rows x D/2
