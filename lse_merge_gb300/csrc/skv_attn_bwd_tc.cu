@@ -235,17 +235,8 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 mbar_arrive_expect_tx(&bb.do_full[st], kTile);
                 for (int c = 0; c < NP; ++c) tma_load_2d(tl.dO[st][c], &map_do, &bb.do_full[st], h * D + c * 64, row);
                 ++nd;
-                // the tile loaded after the next one: into L2 now, so that its load,
-                // issued once this stage is released, does not wait on HBM
-                if (t + 2 < cnt) {
-                    const int row2 = list[t + 2] * BM;
-                    for (int c = 0; c < NP; ++c) {
-                        tma_prefetch_2d(&map_q, h * D + c * 64, row2);
-                        tma_prefetch_2d(&map_do, h * D + c * 64, row2);
-                    }
-                    bulk_prefetch_l2(lse2_hm + int64_t(h) * Qp + row2, BM * 4);
-                    bulk_prefetch_l2(D_hm + int64_t(h) * Qp + row2, BM * 4);
-                }
+                // no L2 prefetch here: a query tile is read by every key tile of its
+                // windows, so its Q and dO are already in L2 (the hints measured slower)
             }
             // every copy issued has landed before the block exits
             mbar_wait(&bb.kv_full, 0, kTeardownWait);
@@ -660,10 +651,9 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_co
         if (lane == 0) {
             int n = 0;       // key tiles whose K load was issued
             int nv = 0;      // key tiles whose V load was issued
-            int64_t x0, xa;
-            // K/V of the tile two ahead go to L2 while this one loads
-            TileIter ahead = it;
-            for (int i = 0; i < 2; ++i) ahead.next(xa);
+            int64_t x0;
+            // no L2 prefetch: the query tiles of a sample walk the same key tiles
+            // close together, so K and V mostly come from L2 already (hints measured slower)
             bool first = true;
             while (it.next(x0)) {
                 if (first) {
@@ -681,11 +671,6 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_co
                 mbar_arrive_expect_tx(&bb.k_full[ks], kTile);
                 for (int c = 0; c < NP; ++c) tma_load_2d(tl.k[ks][c], &map_k, &bb.k_full[ks], h * D + c * 64, (int)x0);
                 ++n;
-                if (ahead.next(xa))
-                    for (int c = 0; c < NP; ++c) {
-                        tma_prefetch_2d(&map_k, h * D + c * 64, (int)xa);
-                        tma_prefetch_2d(&map_v, h * D + c * 64, (int)xa);
-                    }
                 if (n - 1 >= kVStages &&
                     !mbar_wait(&bb.v_empty[vs], ((n - 1 - kVStages) / kVStages) & 1, wait_limit, &bb.abort_flag)) {
                     abort_now();
