@@ -299,6 +299,32 @@ def lse_merge(o_part, lse_part):
     return o, lse
 
 
+def lse_merge_backward(o_part, lse_part, dO, dlse=None):
+    """Backward of the exact merge, per partial  [Split-KV §4.1, Eq. 4; the
+    MERGE_BWD step of Alg. 1's backward].  For a loss with gradients dO (of o)
+    and dlse (of l; None means zero), differentiate o = sum_p w_p o_p and
+    l = log sum_p exp(l_p), where w_p = exp(l_p - l) and dl/dl_p = w_p:
+        d o_p = w_p dO,
+        d l_p = w_p (dO . o_p) - w_p (dO . o) + w_p dlse,
+    the middle term from dw_p/dl_q = w_p (delta_pq - w_q) summed against
+    dO . o_p.  Partials with l_p = -inf get zeros.  Shapes as lse_merge; returns
+    (do_part [P, ...rows..., d], dlse_part [P, ...rows...])."""
+    o_part = np.asarray(o_part, np.float64)
+    lse_part = np.asarray(lse_part, np.float64)
+    g = np.asarray(dO, np.float64)
+    o, lse = lse_merge(o_part, lse_part)
+    fin = np.isfinite(lse_part)
+    lse_safe = np.where(np.isfinite(lse), lse, 0.0)
+    w = np.where(fin, np.exp(np.where(fin, lse_part, 0.0) - lse_safe[None]), 0.0)
+    o_clean = np.where(fin[..., None], o_part, 0.0)
+    dot_p = (g[None] * o_clean).sum(axis=-1)         # dO . o_p
+    dot_o = (g * o).sum(axis=-1)                     # dO . o
+    dl = 0.0 if dlse is None else np.asarray(dlse, np.float64)[None]
+    dlse_part = w * (dot_p - dot_o[None] + dl)
+    do_part = w[..., None] * g[None]
+    return do_part, dlse_part
+
+
 def attention_backward(q, k, v, s, a, B: int, dO, scale: Optional[float] = None,
                        blocks: Optional[Sequence[int]] = None,
                        heads: Optional[Sequence[int]] = None):
