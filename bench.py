@@ -403,6 +403,31 @@ def run_ours(args):
     torch.cuda.synchronize()
     whole_ms = l_s.elapsed_time(l_e) / n_kt
 
+    # the per-partial merge backward (MERGE_BWD of Alg. 1, the route a multi-GPU
+    # build takes) on this step's context partials: timed on its own, not in the step
+    mbwd = None
+    if w.backward:
+        do_part = torch.empty(P, Q, H, d, dtype=torch.float32, device=dev)
+        dlse_part = torch.empty(P, Q, H, dtype=torch.float32, device=dev)
+        op_c, lp_c = o_part[:P], lse_part[:P]
+        skv.lse_merge_bwd(op_c, lp_c, dO, None, do_part=do_part, dlse_part=dlse_part)
+        torch.cuda.synchronize()
+        m_s, m_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        m_s.record()
+        for _ in range(n_kt):
+            skv.lse_merge_bwd(op_c, lp_c, dO, None, do_part=do_part, dlse_part=dlse_part)
+        m_e.record()
+        torch.cuda.synchronize()
+        if skv.stream_status() != 0:
+            raise RuntimeError("device status set by the merge backward")
+        mb_ms = m_s.elapsed_time(m_e) / n_kt
+        fin_c = int(torch.isfinite(lp_c).sum().item())
+        eb_do = 2 if tdt == torch.bfloat16 else 4
+        # lse_part and the finite o_part rows, dO in; dlse_part and do_part out
+        mb_bytes = P * Q * H * 4 + fin_c * d * 4 + Q * H * d * eb_do + P * Q * H * 4 + P * Q * H * d * 4
+        mbwd = {"ms": mb_ms, "bytes": mb_bytes, "gbs": mb_bytes / (mb_ms * 1e-3) / 1e9}
+        del do_part, dlse_part
+
     pairs = useful_pairs_per_head(inp.s, inp.a, w.B) * H
     fwd_flops = 4.0 * d * pairs
     bwd_flops = 8.0 * d * pairs if w.backward else 0.0
@@ -515,6 +540,9 @@ def run_ours(args):
                             "whole_mask_ms_per_step": whole_ms,
                             "fwd": kernels.get("block_local_fwd_kernel"),
                             "bwd": kernels.get("block_local_bwd_kernel")},
+            "merge_bwd": (dict(mbwd, frac_of_hbm=mbwd["gbs"] / hbm, peak_kind=pk_kind,
+                               route="per-partial MERGE_BWD on this step's partials (own pass)")
+                          if mbwd else None),
             "gpu_launches": int(launches),
             "clocks": clk,
             "e2e": e2e,

@@ -201,6 +201,32 @@ SKV_API skv_status skv_lse_merge(const float* o_part, const float* lse_part, int
                          int32_t head_dim, void* o, skv_dtype o_dtype, float* lse, void* stream);
 
 /*
+ * Backward of the exact LSE merge, per partial [Split-KV §4.1, Eq. 4; the
+ * MERGE_BWD step of Alg. 1's backward]: for upstream gradients dO (of o) and
+ * dlse (of lse), with the merged lse and o of skv_lse_merge,
+ * w_p = exp(lse_part[p][r] - lse[r]) and D_p = dO[r] . o_part[p][r]:
+ *   do_part[p][r][:] = w_p * dO[r][:],
+ *   dlse_part[p][r]  = w_p * (D_p - dO[r] . o[r] + dlse[r]),
+ * where dO . o = sum_p w_p D_p is formed from the same partials (the merged o is
+ * not an input, so a rounded copy of it plays no part) and lse is recomputed from
+ * lse_part.  This is the per-rank route a multi-GPU build takes (each rank owns
+ * its partial; sum_p w_p D_p is that route's all-reduce); on one GPU
+ * skv_attn_bwd uses the equivalent merged form instead.  Partials with
+ * lse_part = -inf get do_part = 0 and dlse_part = 0 (their o_part is not read).
+ *   o_part, lse_part  as for skv_lse_merge (o_part 16-byte aligned)
+ *   dO         device [rows][head_dim] of do_dtype (fp32: 16-byte, bf16: 8-byte aligned)
+ *   dlse       device float[rows], or NULL for a zero gradient
+ *   do_part    device float[P][rows][head_dim], written (16-byte aligned), or NULL to skip
+ *   dlse_part  device float[P][rows], written
+ * head_dim as for skv_lse_merge.  Errors: SKV_ERR_INVALID_ARG for P < 1,
+ * rows < 0, a bad dtype or a missing/misaligned pointer; SKV_ERR_UNSUPPORTED
+ * for another head_dim.  Nothing is written on an error.
+ */
+SKV_API skv_status skv_lse_merge_bwd(const float* o_part, const float* lse_part, int32_t P, int64_t rows,
+                                     int32_t head_dim, const void* dO, skv_dtype do_dtype, const float* dlse,
+                                     float* do_part, float* dlse_part, void* stream);
+
+/*
  * Backward of the merged attention for L = sum(dO * o), lse receiving no
  * gradient [Split-KV Alg. 1 lines 12-21]: each virtual rank p produces dq^(p)
  * and the dk_p, dv_p rows of its own chunks (the keys it holds); dq is the sum

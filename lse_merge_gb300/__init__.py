@@ -20,7 +20,7 @@ from . import _lib
 from ._lib import SKV_BF16, SKV_FP32, SkvProblem
 
 __all__ = ["SkvError", "Problem", "chunk_costs", "lpt_order", "contiguous_order", "zigzag_loads",
-           "workspace_bytes", "attn_fwd", "attn_fwd_static", "lse_merge", "attn_bwd", "stream_status", "set_wait_limit",
+           "workspace_bytes", "attn_fwd", "attn_fwd_static", "lse_merge", "lse_merge_bwd", "attn_bwd", "stream_status", "set_wait_limit",
            "forward", "plan", "block_local_fwd", "block_local_bwd"]
 
 
@@ -178,6 +178,23 @@ def lse_merge(o_part: torch.Tensor, lse_part: torch.Tensor, out_dtype: torch.dty
     _check(_lib.load().skv_lse_merge(_ptr(o_part), _ptr(lse_part), P, rows, d, _ptr(o), _dtype_code(o.dtype),
                                      _ptr(lse), _stream()), "skv_lse_merge")
     return o, lse
+
+
+def lse_merge_bwd(o_part: torch.Tensor, lse_part: torch.Tensor, dO: torch.Tensor, dlse: Optional[torch.Tensor] = None,
+                  want_do_part: bool = True, do_part: Optional[torch.Tensor] = None,
+                  dlse_part: Optional[torch.Tensor] = None):
+    """Per-partial backward of Eq. 4 (MERGE_BWD): returns (do_part or None, dlse_part)."""
+    P = o_part.shape[0]
+    d = o_part.shape[-1]
+    rows = lse_part[0].numel()
+    if do_part is None and want_do_part:
+        do_part = torch.empty(o_part.shape, dtype=torch.float32, device=o_part.device)
+    if dlse_part is None:
+        dlse_part = torch.empty(lse_part.shape, dtype=torch.float32, device=o_part.device)
+    _check(_lib.load().skv_lse_merge_bwd(_ptr(o_part), _ptr(lse_part), P, rows, d, _ptr(dO), _dtype_code(dO.dtype),
+                                         _ptr(dlse), _ptr(do_part), _ptr(dlse_part), _stream()),
+           "skv_lse_merge_bwd")
+    return do_part, dlse_part
 
 
 def attn_bwd(prob: Problem, q, k, v, o, lse, dO, rank_of_chunk, dq=None, dk=None, dv=None, workspace=None):

@@ -250,6 +250,26 @@ skv_status skv_lse_merge(const float* o_part, const float* lse_part, int32_t P, 
     return skv_internal::launch_merge(o_part, lse_part, P, rows, head_dim, o, o_dtype, lse, c);
 }
 
+skv_status skv_lse_merge_bwd(const float* o_part, const float* lse_part, int32_t P, int64_t rows,
+                             int32_t head_dim, const void* dO, skv_dtype do_dtype, const float* dlse, float* do_part,
+                             float* dlse_part, void* stream) {
+    if (P < 1 || rows < 0) return SKV_ERR_INVALID_ARG;
+    if (do_dtype != SKV_FP32 && do_dtype != SKV_BF16) return SKV_ERR_INVALID_ARG;
+    switch (head_dim) {
+        case 4: case 8: case 16: case 32: case 64: case 128: case 256: break;
+        default: return SKV_ERR_UNSUPPORTED;
+    }
+    if (rows == 0) return SKV_OK;
+    if (bad_ptr(o_part, 16) || bad_ptr(lse_part, 4) || bad_ptr(dO, do_dtype == SKV_BF16 ? 8 : 16) ||
+        bad_ptr(dlse_part, 4) || (dlse && bad_ptr(dlse, 4)) || (do_part && bad_ptr(do_part, 16)))
+        return SKV_ERR_INVALID_ARG;
+    skv_host::Ctx c;
+    skv_status st = skv_host::get_ctx(stream, c);
+    if (st != SKV_OK) return st;
+    return skv_internal::launch_merge_bwd(o_part, lse_part, P, rows, head_dim, dO, do_dtype, dlse, do_part,
+                                          dlse_part, c);
+}
+
 skv_status skv_attn_bwd(const skv_problem* pb_in, const void* q, const void* k, const void* v, const void* o,
                         const float* lse, const void* dO, const int32_t* rank_of_chunk, float* dq, float* dk,
                         float* dv, void* workspace, size_t ws_bytes, void* stream) {

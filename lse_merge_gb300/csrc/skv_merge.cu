@@ -7,7 +7,8 @@
 // The merge is one HBM pass: G = d/4 lanes own one row (16-byte vectors, rows
 // of 64 or 128 floats are one or half a warp); the row's P log-sum-exps are
 // loaded one per lane, reduced with warp shuffles, and only partials with a
-// finite l_p are read -- so the bytes moved are the algorithmic ones.
+// finite l_p are read -- so the bytes moved are the algorithmic ones.  Its
+// backward per partial (MERGE_BWD) walks the same rows the same way.
 #include <math.h>
 
 #include "skv_common.cuh"
@@ -127,6 +128,157 @@ lse_merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse
     }
 }
 
+__device__ __forceinline__ float4 load4(const float* src) { return __ldcs(reinterpret_cast<const float4*>(src)); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* src) {
+    const uint2 u = *reinterpret_cast<const uint2*>(src);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+// Backward of the merge per partial [Split-KV §4.1, Eq. 4; MERGE_BWD of
+// Alg. 1's backward], for upstream gradients dO (of o) and dlse (of l):
+// with w_p = exp(l_p - l) and D_p = dO . o_p,
+//   do_part[p] = w_p dO,   dlse_part[p] = w_p (D_p - sum_q w_q D_q + dlse),
+// where sum_q w_q D_q = dO . o is taken from the same partials (no rounded o).
+// Lanes as in the merge: G lanes own a row; D_p is a group dot product, four
+// partials in flight; lane 0 of the group parks D_p in dlse_part until the sum
+// over partials is known, then the group's lanes finish their own partials.
+template <int G, int VPL, typename GT>
+__global__ void __launch_bounds__(kThreads)
+lse_merge_bwd_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int P, int64_t rows,
+                     const GT* __restrict__ dO, const float* __restrict__ dlse, float* __restrict__ do_part,
+                     float* __restrict__ dlse_part) {
+    constexpr int D4 = G * VPL;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % G;
+    const int grp = lane / G;
+    constexpr int kRowsPerWarp = 32 / G;
+    constexpr unsigned kGroupBits = (G >= 32) ? 0xffffffffu : ((1u << (G & 31)) - 1u);
+    const unsigned gmask = (G >= 32) ? 0xffffffffu : (kGroupBits << (grp * G));
+    const int64_t warp_global = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t r0 = warp_global * kRowsPerWarp; r0 < rows; r0 += n_warps * kRowsPerWarp) {
+        const int64_t r = r0 + grp;
+        const bool live = r < rows;
+        // the merged l, exactly as the forward merge forms it
+        float mx = -INFINITY;
+        for (int p = sub; p < P; p += G) {
+            const float l = live ? __ldcs(lse_part + int64_t(p) * rows + r) : -INFINITY;
+            mx = fmaxf(mx, l);
+        }
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(gmask, mx, off));
+        float den = 0.f;
+        if (mx != -INFINITY) {
+            for (int p = sub; p < P; p += G) {
+                const float l = __ldcs(lse_part + int64_t(p) * rows + r);
+                den += (l == -INFINITY) ? 0.f : __expf(l - mx);
+            }
+        }
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) den += __shfl_xor_sync(gmask, den, off);
+        const float L = (mx == -INFINITY) ? -INFINITY : mx + __logf(den);
+        const bool any = live && L != -INFINITY;
+        float4 g[VPL];
+#pragma unroll
+        for (int t = 0; t < VPL; ++t) g[t] = any ? load4(dO + r * (4 * D4) + 4 * (sub + t * G)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        // D_p for every finite partial, and sum_p w_p D_p
+        float dot_o = 0.f;
+        if (any) {
+            for (int pb = 0; pb < P; pb += G) {
+                const int p_me = pb + sub;
+                const float l_me = p_me < P ? __ldcs(lse_part + int64_t(p_me) * rows + r) : -INFINITY;
+                const float w_me = (l_me == -INFINITY) ? 0.f : __expf(l_me - L);
+                unsigned fin = __ballot_sync(gmask, l_me != -INFINITY);
+                if (G < 32) fin = (fin >> (grp * G)) & kGroupBits;
+                while (fin) {
+                    int ps[4];
+                    float ws[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        ps[u] = -1;
+                        ws[u] = 0.f;
+                        if (fin) {
+                            const int b = __ffs(fin) - 1;
+                            fin &= fin - 1;
+                            ps[u] = pb + b;
+                            ws[u] = __shfl_sync(gmask, w_me, grp * G + b);
+                        } else {
+                            __shfl_sync(gmask, w_me, grp * G);   // keep the group converged
+                        }
+                    }
+                    float dot[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        dot[u] = 0.f;
+                        if (ps[u] >= 0) {
+                            const float4* src = reinterpret_cast<const float4*>(o_part + (int64_t(ps[u]) * rows + r) * (4 * D4));
+#pragma unroll
+                            for (int t = 0; t < VPL; ++t) {
+                                const float4 x = __ldcs(src + sub + t * G);
+                                dot[u] = fmaf(g[t].x, x.x, fmaf(g[t].y, x.y, fmaf(g[t].z, x.z, fmaf(g[t].w, x.w, dot[u]))));
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int off = G / 2; off > 0; off >>= 1)
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) dot[u] += __shfl_xor_sync(gmask, dot[u], off);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        dot_o = fmaf(ws[u], dot[u], dot_o);
+                        if (sub == 0 && ps[u] >= 0) dlse_part[int64_t(ps[u]) * rows + r] = dot[u];
+                    }
+                }
+            }
+        }
+        __syncwarp(gmask);
+        const float dl = (any && dlse) ? dlse[r] : 0.f;
+        if (live) {
+            for (int p = sub; p < P; p += G) {
+                const float l = __ldcs(lse_part + int64_t(p) * rows + r);
+                const bool f = any && l != -INFINITY;
+                float* dst = dlse_part + int64_t(p) * rows + r;
+                *dst = f ? __expf(l - L) * (*dst - dot_o + dl) : 0.f;
+            }
+        }
+        if (do_part && live) {
+            for (int p = 0; p < P; ++p) {
+                const float l = __ldcs(lse_part + int64_t(p) * rows + r);
+                const float w = (any && l != -INFINITY) ? __expf(l - L) : 0.f;
+                float* dst = do_part + (int64_t(p) * rows + r) * (4 * D4);
+#pragma unroll
+                for (int t = 0; t < VPL; ++t)
+                    store4(dst + 4 * (sub + t * G), make_float4(w * g[t].x, w * g[t].y, w * g[t].z, w * g[t].w));
+            }
+        }
+    }
+}
+
+template <typename GT>
+skv_status merge_bwd_dispatch(const float* o_part, const float* lse_part, int P, int64_t rows, int d, const GT* dO,
+                              const float* dlse, float* do_part, float* dlse_part, const skv_host::Ctx& c) {
+    int blocks = c.num_sms * 8;
+    const int64_t max_blocks = (rows + (kThreads / 32) - 1) / (kThreads / 32);
+    if (blocks > max_blocks) blocks = (int)(max_blocks > 0 ? max_blocks : 1);
+#define SKV_MB(G_, V_) \
+    lse_merge_bwd_kernel<G_, V_, GT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, dO, dlse, do_part, dlse_part)
+    switch (d) {
+        case 64:  SKV_MB(16, 1); break;
+        case 128: SKV_MB(32, 1); break;
+        case 256: SKV_MB(32, 2); break;
+        case 32:  SKV_MB(8, 1); break;
+        case 16:  SKV_MB(4, 1); break;
+        case 8:   SKV_MB(2, 1); break;
+        case 4:   SKV_MB(1, 1); break;
+        default: return SKV_ERR_UNSUPPORTED;
+    }
+#undef SKV_MB
+    SKV_LAUNCHED();
+    return SKV_OK;
+}
+
 template <typename OT>
 skv_status merge_dispatch(const float* o_part, const float* lse_part, int P, int64_t rows, int d, OT* o,
                           float* lse, const skv_host::Ctx& c) {
@@ -210,6 +362,17 @@ skv_status launch_merge(const float* o_part, const float* lse_part, int P, int64
                             : merge_dispatch(o_part, lse_part, P, rows, d, static_cast<float*>(o), lse, c);
     skv_host::timer_end(skv_host::kTimeMerge, c.stream);
     return st;
+}
+
+skv_status launch_merge_bwd(const float* o_part, const float* lse_part, int P, int64_t rows, int d, const void* dO,
+                            skv_dtype do_dtype, const float* dlse, float* do_part, float* dlse_part,
+                            const skv_host::Ctx& c) {
+    if (rows == 0) return SKV_OK;
+    return do_dtype == SKV_BF16
+               ? merge_bwd_dispatch(o_part, lse_part, P, rows, d, static_cast<const __nv_bfloat16*>(dO), dlse,
+                                    do_part, dlse_part, c)
+               : merge_bwd_dispatch(o_part, lse_part, P, rows, d, static_cast<const float*>(dO), dlse, do_part,
+                                    dlse_part, c);
 }
 
 skv_status launch_bwd_prep(const void* o, const void* dO, const float* lse, skv_dtype dt, int64_t Qn, int64_t Qp,

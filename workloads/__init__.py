@@ -202,3 +202,23 @@ def random_small(seed: int, n_samples: int, sample_len: int, anchors_per_sample:
     hi = sample_len if anchor_hi is None else anchor_hi
     return Workload(f"small_{seed}", seed, n_samples, sample_len, anchors_per_sample, lo, hi,
                     B, H, d, m, P, dtype, 1.0 if dtype == "fp32" else 0.5, 1.0, order, True)
+
+
+def merge_partials(seed: int, P: int, rows: int, d: int, do_dtype: str = "fp32", frac_empty: float = 0.2,
+                   device: str = "cpu"):
+    """Seeded inputs of the merge and its backward: (o_part fp32 [P, rows, d],
+    lse_part fp32 [P, rows], dO [rows, d] in do_dtype, dlse fp32 [rows]).
+    A share frac_empty of the partials is empty (lse_part = -inf), and the last
+    row has every partial empty.  Draw order: o_part -> lse_part -> empty mask ->
+    dO -> dlse, one torch generator on `device` (large cases draw on the GPU)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    o_part = torch.randn(P, rows, d, generator=g, device=device)
+    lse_part = torch.randn(P, rows, generator=g, device=device) * 3.0
+    empty = torch.rand(P, rows, generator=g, device=device) < frac_empty
+    if rows > 0:
+        empty[:, rows - 1] = True
+    lse_part = lse_part.masked_fill(empty, float("-inf"))
+    dO = torch.randn(rows, d, generator=g, device=device).to(torch.float32 if do_dtype == "fp32" else torch.bfloat16)
+    dlse = torch.randn(rows, generator=g, device=device)
+    return o_part, lse_part, dO, dlse
