@@ -236,21 +236,28 @@ lse_merge_bwd_kernel(const float* __restrict__ o_part, const float* __restrict__
         __syncwarp(gmask);
         const float dl = (any && dlse) ? dlse[r] : 0.f;
         if (live) {
-            for (int p = sub; p < P; p += G) {
-                const float l = __ldcs(lse_part + int64_t(p) * rows + r);
-                const bool f = any && l != -INFINITY;
-                float* dst = dlse_part + int64_t(p) * rows + r;
-                *dst = f ? __expf(l - L) * (*dst - dot_o + dl) : 0.f;
-            }
-        }
-        if (do_part && live) {
-            for (int p = 0; p < P; ++p) {
-                const float l = __ldcs(lse_part + int64_t(p) * rows + r);
-                const float w = (any && l != -INFINITY) ? __expf(l - L) : 0.f;
-                float* dst = do_part + (int64_t(p) * rows + r) * (4 * D4);
+            // lane b of the group finishes partial pb + b and hands its w_p to the
+            // group for the do_part rows
+            for (int pb = 0; pb < P; pb += G) {
+                const int p_me = pb + sub;
+                float w_me = 0.f;
+                if (p_me < P) {
+                    const float l = __ldcs(lse_part + int64_t(p_me) * rows + r);
+                    const bool f = any && l != -INFINITY;
+                    float* dst = dlse_part + int64_t(p_me) * rows + r;
+                    w_me = f ? __expf(l - L) : 0.f;
+                    *dst = f ? w_me * (*dst - dot_o + dl) : 0.f;
+                }
+                if (do_part) {
+                    const int n = P - pb < G ? P - pb : G;
+                    for (int b = 0; b < n; ++b) {
+                        const float w = __shfl_sync(gmask, w_me, grp * G + b);
+                        float* dst = do_part + (int64_t(pb + b) * rows + r) * (4 * D4);
 #pragma unroll
-                for (int t = 0; t < VPL; ++t)
-                    store4(dst + 4 * (sub + t * G), make_float4(w * g[t].x, w * g[t].y, w * g[t].z, w * g[t].w));
+                        for (int t = 0; t < VPL; ++t)
+                            store4(dst + 4 * (sub + t * G), make_float4(w * g[t].x, w * g[t].y, w * g[t].z, w * g[t].w));
+                    }
+                }
             }
         }
     }
