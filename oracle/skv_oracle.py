@@ -194,18 +194,31 @@ def chunk_key_mask(rank_of_chunk, p: int, m: int, S: int) -> np.ndarray:
     return keys
 
 
-class _Heads:
-    """Per-head fp64 copies of k, v (converted lazily, one head at a time)."""
+def kv_head(h: int, H: int, Hkv: int) -> int:
+    """Grouped-query layouts [Split-KV Table 2: 32 query heads over 4 or 8
+    key/value heads]: query head h attends with key/value head h // (H / Hkv);
+    with Hkv = H this is the identity."""
+    return h // (H // Hkv)
 
-    def __init__(self, k, v):
+
+class _Heads:
+    """Per-head fp64 copies of k, v (converted lazily, one head at a time),
+    indexed by query head (k, v may hold fewer, grouped, heads)."""
+
+    def __init__(self, k, v, H: Optional[int] = None):
         self.k, self.v = k, v
+        self.H = k.shape[1] if H is None else H
         self._h, self._kh, self._vh = None, None, None
 
+    def head(self, h):
+        return kv_head(h, self.H, self.k.shape[1])
+
     def get(self, h):
-        if self._h != h:
-            self._kh = _np64(self.k[:, h, :])
-            self._vh = _np64(self.v[:, h, :])
-            self._h = h
+        c = self.head(h)
+        if self._h != c:
+            self._kh = _np64(self.k[:, c, :])
+            self._vh = _np64(self.v[:, c, :])
+            self._h = c
         return self._kh, self._vh
 
 
@@ -243,7 +256,7 @@ def attention_forward(q, k, v, s, a, B: int, scale: Optional[float] = None,
         scale = 1.0 / math.sqrt(d)
     o = np.zeros((Qn, H, d))
     lse = np.full((Qn, H), NEG_INF)
-    kv = _Heads(k, v)
+    kv = _Heads(k, v, H)
     for h in (range(H) if heads is None else heads):
         kh, vh = kv.get(h)
         for i in (range(N) if blocks is None else blocks):
@@ -344,11 +357,12 @@ def attention_backward(q, k, v, s, a, B: int, dO, scale: Optional[float] = None,
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq = np.zeros((Qn, H, d))
-    dk = np.zeros((S, H, d))
-    dv = np.zeros((S, H, d))
-    kv = _Heads(k, v)
+    dk = np.zeros((S, k.shape[1], d))
+    dv = np.zeros((S, k.shape[1], d))
+    kv = _Heads(k, v, H)
     for h in (range(H) if heads is None else heads):
         kh, vh = kv.get(h)
+        c = kv.head(h)
         for i in (range(N) if blocks is None else blocks):
             rows = slice(i * B, (i + 1) * B)
             mrow = mask_row(int(s[i]), int(a[i]), S)
@@ -357,33 +371,35 @@ def attention_backward(q, k, v, s, a, B: int, dO, scale: Optional[float] = None,
             z = np.where(mrow[None, :], scale * (qb @ kh.T), NEG_INF)
             e, ssum, l_rows, empty = _softmax_stats(z)
             Pm = np.where(empty[:, None], 0.0, e / np.where(empty, 1.0, ssum)[:, None])
-            dv[:, h, :] += Pm.T @ gb
+            dv[:, c, :] += Pm.T @ gb
             dP = gb @ vh.T
             D = (Pm * dP).sum(axis=1)
             dS = Pm * (dP - D[:, None])
             dq[rows, h, :] = scale * (dS @ kh)
-            dk[:, h, :] += scale * (dS.T @ qb)
+            dk[:, c, :] += scale * (dS.T @ qb)
     return dq, dk, dv
 
 
 def backward_key_rows(q, k, v, s, a, B: int, dO, keys: Sequence[int],
                       heads: Sequence[int], scale: Optional[float] = None):
-    """dk, dv at the listed context keys only, for the listed heads (same
-    definition as attention_backward; only the blocks whose window holds one
-    of the keys contribute, and each of those rows needs its full-row l_r and
-    D_r).  Returns (dk [len(keys), len(heads), d], dv [...])."""
+    """dk, dv at the listed context keys only, for the listed key/value heads
+    (same definition as attention_backward, each head summed over its query
+    heads; only the blocks whose window holds one of the keys contribute, and
+    each of those rows needs its full-row l_r and D_r).
+    Returns (dk [len(keys), len(heads), d], dv [...])."""
     s, a = _npi(s), _npi(a)
     N = len(s)
-    d = q.shape[2]
+    H, d = q.shape[1], q.shape[2]
     S = k.shape[0]
+    g = H // k.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     keys = list(keys)
     kidx = np.asarray(keys, np.int64)
     dk = np.zeros((len(keys), len(heads), d))
     dv = np.zeros((len(keys), len(heads), d))
-    kv = _Heads(k, v)
-    for hi, h in enumerate(heads):
+    kv = _Heads(k, v, H)
+    for hi, h in ((hi, h) for hi, c in enumerate(heads) for h in range(c * g, (c + 1) * g)):
         kh, vh = kv.get(h)
         for i in range(N):
             if not np.any((s[i] <= kidx) & (kidx < a[i])):
@@ -423,9 +439,9 @@ def partitioned_backward(q, k, v, s, a, B: int, dO, rank_of_chunk, m: int, P: in
     o, lse = lse_merge(o_part, lse_part)
     g = _np64(dO)
     dq_parts = np.zeros((P, Qn, H, d))
-    dk = np.zeros((S, H, d))
-    dv = np.zeros((S, H, d))
-    kv = _Heads(k, v)
+    dk = np.zeros((S, k.shape[1], d))
+    dv = np.zeros((S, k.shape[1], d))
+    kv = _Heads(k, v, H)
     for p in range(P):
         km = chunk_key_mask(rank_of_chunk, p, m, S)
         for h in range(H):
@@ -446,8 +462,8 @@ def partitioned_backward(q, k, v, s, a, B: int, dO, rank_of_chunk, m: int, P: in
                 dz = Pp * (do_p @ vh.T - (do_p * o_part[p, rows, h, :]).sum(1)[:, None]) \
                     + dl_p[:, None] * Pp
                 dq_parts[p, rows, h, :] = scale * (dz @ kh)
-                dk[:, h, :] += scale * (dz.T @ qb)
-                dv[:, h, :] += Pp.T @ do_p
+                dk[:, kv.head(h), :] += scale * (dz.T @ qb)
+                dv[:, kv.head(h), :] += Pp.T @ do_p
     return dq_parts.sum(axis=0), dk, dv, dq_parts
 
 
@@ -458,8 +474,9 @@ def partitioned_backward(q, k, v, s, a, B: int, dO, rank_of_chunk, m: int, P: in
 # Reading: besides its context window, block i attends bidirectionally to the B
 # tokens of its own block [Split-KV §3.1, Fig. 1 caption; the N B^2 term of
 # T_attn in §4.1].  Those tokens' keys and values are the drafter's own
-# projections of the block positions, so they arrive as two more tensors laid
-# out like q: k_blk, v_blk [Q, H, d], rows [iB, iB+B) belonging to block i.
+# projections of the block positions, so they arrive as two more tensors with
+# q's rows: k_blk, v_blk [Q, Hkv, d], rows [iB, iB+B) belonging to block i (Hkv
+# key/value heads, = H without grouped queries).
 # They are disjoint from every context chunk, so their (o, l) is one more
 # partial of Eq. 4.
 
@@ -477,10 +494,11 @@ def block_local_forward(q, k_blk, v_blk, B: int, scale: Optional[float] = None,
     for h in (range(H) if heads is None else heads):
         for i in range(N):
             rows = slice(i * B, (i + 1) * B)
-            z = scale * (_np64(q[rows, h, :]) @ _np64(k_blk[rows, h, :]).T)
+            c = kv_head(h, H, k_blk.shape[1])
+            z = scale * (_np64(q[rows, h, :]) @ _np64(k_blk[rows, c, :]).T)
             e, ssum, l_rows, _ = _softmax_stats(z)
             lse[rows, h] = l_rows
-            o[rows, h, :] = (e @ _np64(v_blk[rows, h, :])) / ssum[:, None]
+            o[rows, h, :] = (e @ _np64(v_blk[rows, c, :])) / ssum[:, None]
     return o, lse
 
 
@@ -498,13 +516,14 @@ def full_mask_forward(q, k, v, k_blk, v_blk, s, a, B: int, scale: Optional[float
         scale = 1.0 / math.sqrt(d)
     o = np.zeros((Qn, H, d))
     lse = np.full((Qn, H), NEG_INF)
-    kv = _Heads(k, v)
+    kv = _Heads(k, v, H)
     for h in (range(H) if heads is None else heads):
         kh, vh = kv.get(h)
+        c = kv.head(h)
         for i in (range(N) if blocks is None else blocks):
             rows = slice(i * B, (i + 1) * B)
-            keys = np.concatenate([kh, _np64(k_blk[rows, h, :])])
-            vals = np.concatenate([vh, _np64(v_blk[rows, h, :])])
+            keys = np.concatenate([kh, _np64(k_blk[rows, c, :])])
+            vals = np.concatenate([vh, _np64(v_blk[rows, c, :])])
             visible = np.concatenate([mask_row(int(s[i]), int(a[i]), S), np.ones(B, dtype=bool)])
             z = np.where(visible[None, :], scale * (_np64(q[rows, h, :]) @ keys.T), NEG_INF)
             e, ssum, l_rows, _ = _softmax_stats(z)
@@ -541,19 +560,20 @@ def context_backward_given(q, k, v, s, a, B: int, dO, o, lse, scale: Optional[fl
         scale = 1.0 / math.sqrt(d)
     o, lse, g = _np64(o), _np64(lse), _np64(dO)
     dq = np.zeros((Qn, H, d))
-    dk = np.zeros((S, H, d))
-    dv = np.zeros((S, H, d))
-    kv = _Heads(k, v)
+    dk = np.zeros((S, k.shape[1], d))
+    dv = np.zeros((S, k.shape[1], d))
+    kv = _Heads(k, v, H)
     for h in (range(H) if heads is None else heads):
         kh, vh = kv.get(h)
+        c = kv.head(h)
         for i in (range(N) if blocks is None else blocks):
             rows = slice(i * B, (i + 1) * B)
             mrow = mask_row(int(s[i]), int(a[i]), S)[None, :]
             gq, gk, gv = _given_backward(_np64(q[rows, h, :]), kh, vh, g[rows, h, :], o[rows, h, :],
                                          lse[rows, h], mrow, scale)
             dq[rows, h, :] = gq
-            dk[:, h, :] += gk
-            dv[:, h, :] += gv
+            dk[:, c, :] += gk
+            dv[:, c, :] += gv
     return dq, dk, dv
 
 
@@ -561,25 +581,28 @@ def block_local_backward(q, k_blk, v_blk, dO, o, lse, B: int, scale: Optional[fl
                          blocks: Optional[Sequence[int]] = None, heads: Optional[Sequence[int]] = None):
     """The block-local part of the same gradients: rows of block i over the
     block's own keys with the merged o, lse.  Returns (dq_local [Q,H,d],
-    dk_blk [Q,H,d], dv_blk [Q,H,d]); the full dq is the context dq plus dq_local."""
+    dk_blk [Q,Hkv,d], dv_blk [Q,Hkv,d]; a key/value head sums its query heads);
+    the full dq is the context dq plus dq_local."""
     Qn, H, d = q.shape
     N = Qn // B
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     o, lse, g = _np64(o), _np64(lse), _np64(dO)
+    Hkv = k_blk.shape[1]
     dq = np.zeros((Qn, H, d))
-    dk = np.zeros((Qn, H, d))
-    dv = np.zeros((Qn, H, d))
+    dk = np.zeros((Qn, Hkv, d))
+    dv = np.zeros((Qn, Hkv, d))
     allvis = np.ones((1, B), dtype=bool)
     for h in (range(H) if heads is None else heads):
+        c = kv_head(h, H, Hkv)
         for i in (range(N) if blocks is None else blocks):
             rows = slice(i * B, (i + 1) * B)
-            gq, gk, gv = _given_backward(_np64(q[rows, h, :]), _np64(k_blk[rows, h, :]),
-                                         _np64(v_blk[rows, h, :]), g[rows, h, :], o[rows, h, :],
+            gq, gk, gv = _given_backward(_np64(q[rows, h, :]), _np64(k_blk[rows, c, :]),
+                                         _np64(v_blk[rows, c, :]), g[rows, h, :], o[rows, h, :],
                                          lse[rows, h], allvis, scale)
             dq[rows, h, :] = gq
-            dk[rows, h, :] = gk
-            dv[rows, h, :] = gv
+            dk[rows, c, :] += gk
+            dv[rows, c, :] += gv
     return dq, dk, dv
 
 
