@@ -285,7 +285,7 @@ def run_ours(args):
     q, k, v = inp.q, inp.k, inp.v
     kb, vb = block_kv(w, device=str(dev))       # the block tokens' own keys / values
     dO = inp.dO if w.backward else None
-    prob = skv.Problem(s, a, w.B, w.H, w.d, w.S, w.m, w.P, tdt)
+    prob = skv.Problem(s, a, w.B, w.H, w.d, w.S, w.m, w.P, tdt, n_kv_heads=w.Hkv)
     P, Q, H, d = w.P, w.Q, w.H, w.d
     # P rank partials (+ slot P for the block-local partial of the separate pass)
     o_part = torch.empty(P + 1, Q, H, d, dtype=torch.float32, device=dev)
@@ -294,10 +294,10 @@ def run_ours(args):
     lse = torch.empty(Q, H, dtype=torch.float32, device=dev)
     if w.backward:
         dq = torch.empty(Q, H, d, dtype=torch.float32, device=dev)
-        dk = torch.empty(w.S, H, d, dtype=torch.float32, device=dev)
-        dv = torch.empty(w.S, H, d, dtype=torch.float32, device=dev)
-        dkb = torch.empty(Q, H, d, dtype=torch.float32, device=dev)
-        dvb = torch.empty(Q, H, d, dtype=torch.float32, device=dev)
+        dk = torch.empty(w.S, w.KVH, d, dtype=torch.float32, device=dev)
+        dv = torch.empty(w.S, w.KVH, d, dtype=torch.float32, device=dev)
+        dkb = torch.empty(Q, w.KVH, d, dtype=torch.float32, device=dev)
+        dvb = torch.empty(Q, w.KVH, d, dtype=torch.float32, device=dev)
         ws_b = torch.empty(skv.workspace_bytes(prob, 1), dtype=torch.uint8, device=dev)
     ws_f = torch.empty(skv.workspace_bytes(prob, 0), dtype=torch.uint8, device=dev)
     costs = torch.empty(w.n_chunks, dtype=torch.int64, device=dev)
@@ -450,8 +450,9 @@ def run_ours(args):
     # dk_blk, dv_blk out)
     eb = 2 if tdt == torch.bfloat16 else 4
     rows_h = Q * H
-    local_bytes = {"block_local_fwd_kernel": rows_h * (3 * d * eb + d * 4 + 4),
-                   "block_local_bwd_kernel": rows_h * (5 * d * eb + 4 + 2 * d * 4 + 2 * d * 4)}
+    rows_kv = Q * w.KVH                      # k_blk, v_blk, dk_blk, dv_blk rows (grouped heads)
+    local_bytes = {"block_local_fwd_kernel": rows_h * (d * eb + d * 4 + 4) + rows_kv * 2 * d * eb,
+                   "block_local_bwd_kernel": rows_h * (3 * d * eb + 4 + 2 * d * 4) + rows_kv * (2 * d * eb + 2 * d * 4)}
     kernels = {}
     for i, nm in enumerate(kt_names):
         if kt_ms[i]:
@@ -480,8 +481,8 @@ def run_ours(args):
         h_o = torch.empty(Q, H, d, dtype=tdt, pin_memory=True)
         h_lse = torch.empty(Q, H, dtype=torch.float32, pin_memory=True)
         h_dq = torch.empty(Q, H, d, dtype=torch.float32, pin_memory=True)
-        h_dk = torch.empty(w.S, H, d, dtype=torch.float32, pin_memory=True)
-        h_dv = torch.empty(w.S, H, d, dtype=torch.float32, pin_memory=True)
+        h_dk = torch.empty(w.S, w.KVH, d, dtype=torch.float32, pin_memory=True)
+        h_dv = torch.empty(w.S, w.KVH, d, dtype=torch.float32, pin_memory=True)
         h_in = [(x.cpu().pin_memory(), x) for x in (s, a, q, k, v, dO)]
         h_out = [(o, h_o), (lse, h_lse), (dq, h_dq), (dk, h_dk), (dv, h_dv)]
         bi = sum(x.numel() * x.element_size() for x, _ in h_in)
@@ -521,7 +522,8 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if tdt == torch.bfloat16 else "f32", "data": "synthetic",
-            "config": {"workload": w.name, "b": w.n_samples, "S": w.S, "Q": w.Q, "B": w.B, "H": H, "d": d,
+            "config": {"workload": w.name, "b": w.n_samples, "S": w.S, "Q": w.Q, "B": w.B, "H": H, "Hkv": w.KVH,
+                       "d": d,
                        "m": w.m, "P": P, "J": w.J, "order": w.order,
                        "l2": "inputs larger than L2 (K+V alone exceed 129 MB)",
                        "mask": "context windows (block-local term: block_local object)",

@@ -64,6 +64,10 @@ typedef enum skv_dtype {
  * Block i (rows [i*B, (i+1)*B)) attends exactly the context keys
  * s_i <= x < a_i.  The context [0, S) is cut into S/m chunks
  * [j*m, (j+1)*m); P virtual ranks hold J chunks each (P*J*m == S).
+ * With grouped-query attention (the drafters of Table 2: 32 query heads over
+ * 4 or 8 key/value heads) k, v, dk, dv and the block-local k_blk, v_blk,
+ * dk_blk, dv_blk have Hkv heads in place of H; every shape below written with
+ * [H] for those tensors means [Hkv].
  */
 typedef struct skv_problem {
     int32_t B;            /* block size: query rows per anchor, 1..128        */
@@ -78,6 +82,9 @@ typedef struct skv_problem {
     const int32_t* a;     /* device [N]: anchor of block i, s_i <= a_i <= S    */
     skv_dtype dtype;      /* dtype of q, k, v, o (merged) and dO               */
     float scale;          /* softmax scale; 0 selects 1/sqrt(head_dim)         */
+    int32_t n_kv_heads;   /* Hkv: heads of k, v (and dk, dv); 0 selects H.     */
+                          /* Grouped-query layout [Table 2]: H % Hkv == 0 and  */
+                          /* query head h reads key/value head h / (H / Hkv)   */
 } skv_problem;
 
 /*

@@ -62,7 +62,7 @@ class Problem:
     tensors [N] (sample start and anchor of each block)."""
 
     def __init__(self, s: torch.Tensor, a: torch.Tensor, B: int, n_heads: int, head_dim: int, S: int, m: int,
-                 P: int, dtype: torch.dtype = torch.bfloat16, scale: float = 0.0):
+                 P: int, dtype: torch.dtype = torch.bfloat16, scale: float = 0.0, n_kv_heads: int = 0):
         if s.dtype != torch.int32 or a.dtype != torch.int32:
             raise ValueError("anchors must be int32")
         if s.numel() != a.numel():
@@ -71,10 +71,11 @@ class Problem:
         J = n_chunks // P if P else 0
         self.s, self.a = s, a          # keep the device buffers alive
         self.B, self.N, self.H, self.d, self.S, self.m, self.P, self.J = B, s.numel(), n_heads, head_dim, S, m, P, J
+        self.Hkv = n_kv_heads or n_heads     # heads of k, v, dk, dv (grouped-query layouts)
         self.dtype = dtype
         self.c = SkvProblem(B, s.numel(), n_heads, head_dim, S, m, P, J,
                             _ptr(s) if s.numel() else None, _ptr(a) if a.numel() else None,
-                            _dtype_code(dtype), float(scale))
+                            _dtype_code(dtype), float(scale), int(n_kv_heads))
 
     @property
     def Q(self) -> int:
@@ -201,8 +202,8 @@ def attn_bwd(prob: Problem, q, k, v, o, lse, dO, rank_of_chunk, dq=None, dk=None
     """(dq, dk, dv) fp32 of L = sum(dO * o)."""
     dev = k.device
     dq = torch.empty(prob.Q, prob.H, prob.d, dtype=torch.float32, device=dev) if dq is None else dq
-    dk = torch.empty(prob.S, prob.H, prob.d, dtype=torch.float32, device=dev) if dk is None else dk
-    dv = torch.empty(prob.S, prob.H, prob.d, dtype=torch.float32, device=dev) if dv is None else dv
+    dk = torch.empty(prob.S, prob.Hkv, prob.d, dtype=torch.float32, device=dev) if dk is None else dk
+    dv = torch.empty(prob.S, prob.Hkv, prob.d, dtype=torch.float32, device=dev) if dv is None else dv
     ws = _workspace(prob, 1, workspace)
     _check(_lib.load().skv_attn_bwd(prob.ref(), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
                                     _ptr(rank_of_chunk), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
@@ -225,8 +226,8 @@ def block_local_bwd(prob: Problem, q, k_blk, v_blk, o, lse, dO, dq, dk_blk=None,
     """Adds the block-local part to dq (fp32, holding the context part) and returns
     (dq, dk_blk, dv_blk); o, lse are the merged results of the whole mask."""
     dev = q.device
-    dk_blk = torch.empty(prob.Q, prob.H, prob.d, dtype=torch.float32, device=dev) if dk_blk is None else dk_blk
-    dv_blk = torch.empty(prob.Q, prob.H, prob.d, dtype=torch.float32, device=dev) if dv_blk is None else dv_blk
+    dk_blk = torch.empty(prob.Q, prob.Hkv, prob.d, dtype=torch.float32, device=dev) if dk_blk is None else dk_blk
+    dv_blk = torch.empty(prob.Q, prob.Hkv, prob.d, dtype=torch.float32, device=dev) if dv_blk is None else dv_blk
     _check(_lib.load().skv_block_local_bwd(prob.ref(), _ptr(q), _ptr(k_blk), _ptr(v_blk), _ptr(o), _ptr(lse),
                                            _ptr(dO), _ptr(dq), _ptr(dk_blk), _ptr(dv_blk), _stream()),
            "skv_block_local_bwd")

@@ -45,7 +45,7 @@ class SkvProblem(ctypes.Structure):
     _fields_ = [
         ("B", c_int32), ("n_blocks", c_int32), ("n_heads", c_int32), ("head_dim", c_int32),
         ("S", c_int64), ("m", c_int32), ("P", c_int32), ("J", c_int32),
-        ("s", c_void_p), ("a", c_void_p), ("dtype", c_int), ("scale", c_float),
+        ("s", c_void_p), ("a", c_void_p), ("dtype", c_int), ("scale", c_float), ("n_kv_heads", c_int32),
     ]
 
 

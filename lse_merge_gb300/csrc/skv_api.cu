@@ -36,6 +36,9 @@ skv_status validate(const skv_problem* pb, bool attention) {
     if (pb->n_blocks > 0 && (pb->s == nullptr || pb->a == nullptr)) return SKV_ERR_INVALID_ARG;
     if (pb->dtype != SKV_FP32 && pb->dtype != SKV_BF16) return SKV_ERR_INVALID_ARG;
     if (!(pb->scale >= 0.f) || isinf(pb->scale)) return SKV_ERR_INVALID_ARG;
+    if (pb->n_kv_heads < 0 || pb->n_kv_heads > pb->n_heads ||
+        (pb->n_kv_heads > 0 && pb->n_heads % pb->n_kv_heads != 0))
+        return SKV_ERR_INVALID_ARG;
     if (attention) {
         if (pb->head_dim != 64 && pb->head_dim != 128) return SKV_ERR_UNSUPPORTED;
         if (pb->m % 128 != 0) return SKV_ERR_UNSUPPORTED;
@@ -47,6 +50,7 @@ skv_status validate(const skv_problem* pb, bool attention) {
 skv_problem normalized(const skv_problem* pb) {
     skv_problem c = *pb;
     if (c.scale == 0.f) c.scale = 1.0f / sqrtf((float)c.head_dim);
+    if (c.n_kv_heads == 0) c.n_kv_heads = c.n_heads;
     return c;
 }
 
@@ -285,7 +289,7 @@ skv_status skv_attn_bwd(const skv_problem* pb_in, const void* q, const void* k, 
         return SKV_ERR_INVALID_ARG;
     skv_host::Ctx c;
     if ((st = skv_host::get_ctx(stream, c)) != SKV_OK) return st;
-    const int64_t kv_elems = pb.S * pb.n_heads * pb.head_dim;
+    const int64_t kv_elems = pb.S * pb.n_kv_heads * pb.head_dim;
     const bool tc = skv_tc::bwd_supported(pb);
     if (rows == 0 || !tc) {   // the tensor-core kernel writes every dk/dv row itself
         if ((st = skv_internal::launch_zero(dk, kv_elems, c)) != SKV_OK) return st;

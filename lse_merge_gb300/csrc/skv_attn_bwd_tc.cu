@@ -6,9 +6,10 @@
 // P = exp(z - l).  Two kernels:
 //
 //  * attn_bwd_dkdv_tc_kernel -- key-stationary.  One thread block owns a
-//    128-key tile and a head (the tile belongs to exactly one rank, so dk_p and
-//    dv_p rows are written once, no atomics) and walks the query tiles of its
-//    tile-skip list (built by qtile_bounds_kernel / kv_list_kernel; masked-out
+//    128-key tile and a key/value head (the tile belongs to exactly one rank, so
+//    dk_p and dv_p rows are written once, no atomics) and walks, for each query
+//    head of the head's group (one head without grouped queries), the query tiles
+//    of its tile-skip list (built by qtile_bounds_kernel / kv_list_kernel; masked-out
 //    query tiles are never loaded).  Per query tile t:
 //      S^T = K Q_t^T, dP^T = V dO_t^T (SS) -> TMEM A, B
 //      eight warps: P^T = exp2(S^T scale log2e - l2) as bf16 -> TMEM A over the
@@ -127,8 +128,8 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                         const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                         const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
                         const float* __restrict__ lse2_hm, const float* __restrict__ D_hm, int64_t Qp,
-                        const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int64_t Qn, int H,
-                        int64_t S, float scale, float scale_log2, const int4* __restrict__ qtb,
+                        const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int64_t Qn, int Hkv,
+                        int gq, int64_t S, float scale, float scale_log2, const int4* __restrict__ qtb,
                         const int32_t* __restrict__ kv_cnt, const int32_t* __restrict__ kv_list, int n_qt,
                         float* __restrict__ dk, float* __restrict__ dv, int* status, long long wait_limit) {
     extern __shared__ unsigned char smem_raw[];
@@ -143,7 +144,9 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
     KvTiles<D>& tl = sm.t;
     KvBars& bb = sm.b;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int kt = blockIdx.x, h = blockIdx.y;
+    // one key/value head kvh; its gq query heads (grouped-query layouts) are walked
+    // one after the other and all accumulate into the same dK, dV
+    const int kt = blockIdx.x, kvh = blockIdx.y;
     const int64_t x0 = int64_t(kt) * BN;
     constexpr int NP = D / 64;
     constexpr uint32_t kTile = BM * D * 2;
@@ -154,6 +157,7 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
     int cnt = kv_cnt[kt];
     if (*(volatile int*)status == SKV_ERR_TIMEOUT) cnt = 0;   // launch already void: skip the work
     const int32_t* list = kv_list + int64_t(kt) * n_qt;
+    const int n_it = cnt * gq;                       // (query head, query tile) pairs, head-major
 
     if (tid == 0) {
         mbar_init(&bb.kv_full, 1);
@@ -198,14 +202,14 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             prefetch_tensormap(&map_do);
             mbar_arrive_expect_tx(&bb.kv_full, 2 * kTile);
             for (int c = 0; c < NP; ++c) {
-                tma_load_2d(tl.k[c], &map_k, &bb.kv_full, h * D + c * 64, (int)x0);
-                tma_load_2d(tl.v[c], &map_v, &bb.kv_full, h * D + c * 64, (int)x0);
+                tma_load_2d(tl.k[c], &map_k, &bb.kv_full, kvh * D + c * 64, (int)x0);
+                tma_load_2d(tl.v[c], &map_v, &bb.kv_full, kvh * D + c * 64, (int)x0);
             }
             // Q, the tile's metadata (l2, D, bounds) and dO have their own rings: the dK
             // MMA frees Q, the compute warps free the metadata once dS is formed and the
             // dV MMA frees dO; S of a tile needs Q first, so Q runs one stage deeper
             int nq = 0, nm = 0, nd = 0;
-            for (int t = 0; t < cnt; ++t) {
+            for (int t = 0; t < n_it; ++t) {
                 const int sq = t % kQSt, st = t & 1;
                 if (t >= kQSt &&
                     !mbar_wait(&bb.q_empty[sq], ((t - kQSt) / kQSt) & 1, wait_limit, &bb.abort_flag)) {
@@ -213,10 +217,11 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                     break;
                 }
                 if (*(volatile int*)&bb.abort_flag) break;
-                const int qt = list[t];
+                const int hq = kvh * gq + t / cnt;       // query head of this item
+                const int qt = list[t % cnt];
                 const int row = qt * BM;
                 mbar_arrive_expect_tx(&bb.q_full[sq], kTile);
-                for (int c = 0; c < NP; ++c) tma_load_2d(tl.q[sq][c], &map_q, &bb.q_full[sq], h * D + c * 64, row);
+                for (int c = 0; c < NP; ++c) tma_load_2d(tl.q[sq][c], &map_q, &bb.q_full[sq], hq * D + c * 64, row);
                 ++nq;
                 if (t >= 2 && !mbar_wait(&bb.meta_empty[st], ((t - 2) >> 1) & 1, wait_limit, &bb.abort_flag)) {
                     abort_now();
@@ -225,15 +230,15 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 sm.meta[st].qt = qt;                     // made visible by the arrive below
                 sm.meta[st].bnd = qtb[qt];
                 mbar_arrive_expect_tx(&bb.meta_full[st], 2 * BM * 4);
-                bulk_load(sm.meta[st].lse2, lse2_hm + int64_t(h) * Qp + row, BM * 4, &bb.meta_full[st]);
-                bulk_load(sm.meta[st].D, D_hm + int64_t(h) * Qp + row, BM * 4, &bb.meta_full[st]);
+                bulk_load(sm.meta[st].lse2, lse2_hm + int64_t(hq) * Qp + row, BM * 4, &bb.meta_full[st]);
+                bulk_load(sm.meta[st].D, D_hm + int64_t(hq) * Qp + row, BM * 4, &bb.meta_full[st]);
                 ++nm;
                 if (t >= 2 && !mbar_wait(&bb.do_empty[st], ((t - 2) >> 1) & 1, wait_limit, &bb.abort_flag)) {
                     abort_now();
                     break;
                 }
                 mbar_arrive_expect_tx(&bb.do_full[st], kTile);
-                for (int c = 0; c < NP; ++c) tma_load_2d(tl.dO[st][c], &map_do, &bb.do_full[st], h * D + c * 64, row);
+                for (int c = 0; c < NP; ++c) tma_load_2d(tl.dO[st][c], &map_do, &bb.do_full[st], hq * D + c * 64, row);
                 ++nd;
                 // no L2 prefetch here: a query tile is read by every key tile of its
                 // windows, so its Q and dO are already in L2 (the hints measured slower)
@@ -308,9 +313,9 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             //   S_{t+1} -> A  right behind the dV MMAs reading P_t from A
             //   [dS_t stored] dK += dS_t^T Q_t   (dS_t bf16 over the read dP_t)
             //   dP_{t+1} -> B right behind the dK MMAs reading dS_t from B
-            for (int t = 0; ok && t < cnt; ++t) {
+            for (int t = 0; ok && t < n_it; ++t) {
                 const int st = t & 1, sq = t % kQSt, sq1 = (t + 1) % kQSt;
-                const bool more = t + 1 < cnt;
+                const bool more = t + 1 < n_it;
                 // bf16 P^T of query columns [64h, 64h+64) sits in TMEM columns [64h, 64h+32) of
                 // A; it arrives in two parts (query columns [64h, 64h+32), then [64h+32, 64h+64)
                 // of both halves), and the dV MMAs of each part go as soon as it is stored
@@ -376,7 +381,7 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
             if (!got && lane == 0) abort_now();
             return got;
         };
-        for (int t = 0; t < cnt; ++t) {
+        for (int t = 0; t < n_it; ++t) {
             const int st = t & 1;
             if (__any_sync(kAll, *(volatile int*)&bb.abort_flag != 0)) { ok = false; break; }
             if (!uniform_wait(&bb.meta_full[st], (t >> 1) & 1)) { ok = false; break; }
@@ -524,16 +529,16 @@ attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_
                 for (int c = 0; c < kHalf / 32; ++c) {
                     const int p = hf * (kHalf / 32) + c;
                     const uint32_t off = uint32_t(p) * (BN * 128u) + uint32_t(quad * 32) * 128u;
-                    tma_store_2d(&map_dk, stage_k + off, h * D + p * 32, (int)(x0 + quad * 32));
-                    tma_store_2d(&map_dv, stage_v + off, h * D + p * 32, (int)(x0 + quad * 32));
+                    tma_store_2d(&map_dk, stage_k + off, kvh * D + p * 32, (int)(x0 + quad * 32));
+                    tma_store_2d(&map_dv, stage_v + off, kvh * D + p * 32, (int)(x0 + quad * 32));
                 }
                 bulk_commit_group();
                 bulk_wait_read_all();
             }
             __syncwarp();
         } else if (cnt == 0) {
-            float* dkr = dk + (x * H + h) * D + hf * kHalf;
-            float* dvr = dv + (x * H + h) * D + hf * kHalf;
+            float* dkr = dk + (x * Hkv + kvh) * D + hf * kHalf;
+            float* dvr = dv + (x * Hkv + kvh) * D + hf * kHalf;
             const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < kHalf; j += 4) {
@@ -589,7 +594,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_co
                       const __nv_bfloat16* __restrict__ qg, const __nv_bfloat16* __restrict__ dOg,
                       const float* __restrict__ lse2_hm, const float* __restrict__ D_hm, int64_t Qp,
                       const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int64_t Qn, int H,
-                      int64_t S, int m, int P, float scale, float scale_log2, const int4* __restrict__ qtb,
+                      int gq, int64_t S, int m, int P, float scale, float scale_log2, const int4* __restrict__ qtb,
                       skv::RankCSR csr, float* __restrict__ dq, int* status, long long wait_limit) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t base_s = smem_u32(smem_raw);
@@ -603,6 +608,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_co
     QBars& bb = sm.b;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qt = blockIdx.x, h = blockIdx.y;
+    const int kvh = h / gq;                          // key/value head of this query head
     constexpr int NP = D / 64;
     constexpr uint32_t kTile = BM * D * 2;
     const bool stuck_test = wait_limit < 0;
@@ -669,7 +675,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_co
                 }
                 if (*(volatile int*)&bb.abort_flag) break;
                 mbar_arrive_expect_tx(&bb.k_full[ks], kTile);
-                for (int c = 0; c < NP; ++c) tma_load_2d(tl.k[ks][c], &map_k, &bb.k_full[ks], h * D + c * 64, (int)x0);
+                for (int c = 0; c < NP; ++c) tma_load_2d(tl.k[ks][c], &map_k, &bb.k_full[ks], kvh * D + c * 64, (int)x0);
                 ++n;
                 if (n - 1 >= kVStages &&
                     !mbar_wait(&bb.v_empty[vs], ((n - 1 - kVStages) / kVStages) & 1, wait_limit, &bb.abort_flag)) {
@@ -677,7 +683,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_co
                     break;
                 }
                 mbar_arrive_expect_tx(&bb.v_full[vs], kTile);
-                for (int c = 0; c < NP; ++c) tma_load_2d(tl.v[vs][c], &map_v, &bb.v_full[vs], h * D + c * 64, (int)x0);
+                for (int c = 0; c < NP; ++c) tma_load_2d(tl.v[vs][c], &map_v, &bb.v_full[vs], kvh * D + c * 64, (int)x0);
                 ++nv;
             }
             // every copy issued has landed before the block exits
@@ -952,18 +958,20 @@ skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const
     kv_list_kernel<<<(n_kv + 7) / 8, 256, 0, c.stream>>>(w.qtb, n_qt, n_kv, w.cnt, w.list);
     SKV_LAUNCHED();
     CUtensorMap mq, mdo, mk, mv, mdk, mdv;
-    const int64_t cols = int64_t(pb.n_heads) * D;
-    if (!make_map(&mq, q, Qn, cols) || !make_map(&mdo, dO, Qn, cols) || !make_map(&mk, k, pb.S, cols) ||
-        !make_map(&mv, v, pb.S, cols) || !make_map_f32(&mdk, dk, pb.S, cols) || !make_map_f32(&mdv, dv, pb.S, cols))
+    const int64_t cols = int64_t(pb.n_heads) * D, kv_cols = int64_t(pb.n_kv_heads) * D;
+    const int gq = pb.n_heads / pb.n_kv_heads;
+    if (!make_map(&mq, q, Qn, cols) || !make_map(&mdo, dO, Qn, cols) || !make_map(&mk, k, pb.S, kv_cols) ||
+        !make_map(&mv, v, pb.S, kv_cols) || !make_map_f32(&mdk, dk, pb.S, kv_cols) ||
+        !make_map_f32(&mdv, dv, pb.S, kv_cols))
         return SKV_ERR_CUDA;
     const float scale_log2 = pb.scale * 1.4426950408889634f;
     {
         auto kern = attn_bwd_dkdv_tc_kernel<D>;
         SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax));
         skv_host::timer_begin(skv_host::kTimeBwdKV, c.stream);
-        kern<<<dim3((unsigned)n_kv, (unsigned)pb.n_heads), kKvThreads, kSmemMax, c.stream>>>(
-            mq, mdo, mk, mv, mdk, mdv, lse2_hm, D_hm, Qp, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.scale, scale_log2, w.qtb,
-            w.cnt, w.list, n_qt, dk, dv, c.status, c.wait_limit);
+        kern<<<dim3((unsigned)n_kv, (unsigned)pb.n_kv_heads), kKvThreads, kSmemMax, c.stream>>>(
+            mq, mdo, mk, mv, mdk, mdv, lse2_hm, D_hm, Qp, pb.s, pb.a, pb.B, Qn, pb.n_kv_heads, gq, pb.S, pb.scale,
+            scale_log2, w.qtb, w.cnt, w.list, n_qt, dk, dv, c.status, c.wait_limit);
         skv_host::timer_end(skv_host::kTimeBwdKV, c.stream);
         SKV_LAUNCHED();
     }
@@ -973,8 +981,8 @@ skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const
         skv_host::timer_begin(skv_host::kTimeBwdQ, c.stream);
         kern<<<dim3((unsigned)n_qt, (unsigned)pb.n_heads), kQThreads, kSmemMax, c.stream>>>(
             mk, mv, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), lse2_hm, D_hm, Qp,
-            pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.m, pb.P, pb.scale, scale_log2, w.qtb, csr, dq, c.status,
-            c.wait_limit);
+            pb.s, pb.a, pb.B, Qn, pb.n_heads, gq, pb.S, pb.m, pb.P, pb.scale, scale_log2, w.qtb, csr, dq,
+            c.status, c.wait_limit);
         skv_host::timer_end(skv_host::kTimeBwdQ, c.stream);
         SKV_LAUNCHED();
     }

@@ -12,7 +12,8 @@
 // Diffusion Drafters" (§4.1) with an online (running max) softmax.
 // Backward: Alg. 1 lines 15-17 in merged form, P = exp(z - l_global),
 // dS = P (dP - D); dq^(p) is written per rank (summed by the dq-sum pass) and
-// dk, dv accumulate with fp32 atomics (several blocks see the same key).
+// dk, dv accumulate with fp32 atomics (several blocks see the same key; with
+// grouped queries, every query head of a key/value head's group too).
 #include <math.h>
 
 #include "skv_common.cuh"
@@ -50,13 +51,14 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 attn_fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                      const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int n_blocks, int H,
-                     int d, int64_t S, int m, int P, float scale, skv::RankCSR csr, float* __restrict__ o_part,
+                     int Hkv, int d, int64_t S, int m, int P, float scale, skv::RankCSR csr, float* __restrict__ o_part,
                      float* __restrict__ lse_part) {
     extern __shared__ float sm[];
     const int groups = (B + kRows - 1) / kRows;
     const int i = blockIdx.x / groups;
     const int g = blockIdx.x - i * groups;
     const int h = blockIdx.y, p = blockIdx.z;
+    const int kvh = h / (H / Hkv);                   // key/value head (grouped-query layouts)
     const int r0 = i * B + g * kRows;
     const int nr = min(kRows, B - g * kRows);
     const int64_t Qn = int64_t(n_blocks) * B;
@@ -84,8 +86,8 @@ attn_fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
         const int64_t khi = hi < cl + m ? hi : cl + m;
         for (int64_t kt = klo; kt < khi; kt += kKeys) {
             const int nk = (int)((khi - kt) < kKeys ? (khi - kt) : kKeys);
-            load_tile(sk, d + 1, k, kt, nk, H, h, d);
-            load_tile(sv, d + 1, v, kt, nk, H, h, d);
+            load_tile(sk, d + 1, k, kt, nk, Hkv, kvh, d);
+            load_tile(sv, d + 1, v, kt, nk, Hkv, kvh, d);
             __syncthreads();
             for (int e = threadIdx.x; e < kRows * kKeys; e += blockDim.x) {
                 const int r = e / kKeys, c = e % kKeys;
@@ -150,13 +152,14 @@ __global__ void __launch_bounds__(kThreads)
 attn_bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                      const T* __restrict__ dO, const float* __restrict__ lse, const float* __restrict__ Drow,
                      const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int n_blocks, int H,
-                     int d, int64_t S, int m, int P, float scale, skv::RankCSR csr,
+                     int Hkv, int d, int64_t S, int m, int P, float scale, skv::RankCSR csr,
                      float* __restrict__ dq_part, float* __restrict__ dk, float* __restrict__ dv) {
     extern __shared__ float sm[];
     const int groups = (B + kRows - 1) / kRows;
     const int i = blockIdx.x / groups;
     const int g = blockIdx.x - i * groups;
     const int h = blockIdx.y, p = blockIdx.z;
+    const int kvh = h / (H / Hkv);                   // key/value head (grouped-query layouts)
     const int r0 = i * B + g * kRows;
     const int nr = min(kRows, B - g * kRows);
     const int64_t Qn = int64_t(n_blocks) * B;
@@ -190,8 +193,8 @@ attn_bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
         const int64_t khi = hi < cl + m ? hi : cl + m;
         for (int64_t kt = klo; kt < khi; kt += kKeys) {
             const int nk = (int)((khi - kt) < kKeys ? (khi - kt) : kKeys);
-            load_tile(sk, d + 1, k, kt, nk, H, h, d);
-            load_tile(sv, d + 1, v, kt, nk, H, h, d);
+            load_tile(sk, d + 1, k, kt, nk, Hkv, kvh, d);
+            load_tile(sv, d + 1, v, kt, nk, Hkv, kvh, d);
             __syncthreads();
             for (int e = threadIdx.x; e < kRows * kKeys; e += blockDim.x) {
                 const int r = e / kKeys, c = e % kKeys;
@@ -222,7 +225,7 @@ attn_bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
                     gk = fmaf(sds[r * kKeys + c], sq[r * d + t], gk);
                     gv = fmaf(sp[r * kKeys + c], sdo[r * d + t], gv);
                 }
-                const int64_t off = ((kt + c) * H + h) * int64_t(d) + t;
+                const int64_t off = ((kt + c) * Hkv + kvh) * int64_t(d) + t;
                 atomicAdd(dk + off, scale * gk);
                 atomicAdd(dv + off, gv);
             }
@@ -254,14 +257,14 @@ skv_status launch_attn_fwd_simt(const skv_problem& pb, const void* q, const void
         SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         kern<<<simt_grid(pb), kThreads, smem, c.stream>>>(
             static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-            static_cast<const __nv_bfloat16*>(v), pb.s, pb.a, pb.B, pb.n_blocks, pb.n_heads, pb.head_dim, pb.S,
+            static_cast<const __nv_bfloat16*>(v), pb.s, pb.a, pb.B, pb.n_blocks, pb.n_heads, pb.n_kv_heads, pb.head_dim, pb.S,
             pb.m, pb.P, scale, csr, o_part, lse_part);
     } else {
         auto kern = attn_fwd_simt_kernel<float>;
         SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         kern<<<simt_grid(pb), kThreads, smem, c.stream>>>(
             static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), pb.s, pb.a,
-            pb.B, pb.n_blocks, pb.n_heads, pb.head_dim, pb.S, pb.m, pb.P, scale, csr, o_part, lse_part);
+            pb.B, pb.n_blocks, pb.n_heads, pb.n_kv_heads, pb.head_dim, pb.S, pb.m, pb.P, scale, csr, o_part, lse_part);
     }
     SKV_LAUNCHED();
     return SKV_OK;
@@ -278,13 +281,13 @@ skv_status launch_attn_bwd_simt(const skv_problem& pb, const void* q, const void
         kern<<<simt_grid(pb), kThreads, smem, c.stream>>>(
             static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
             static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(dO), lse, D, pb.s, pb.a, pb.B,
-            pb.n_blocks, pb.n_heads, pb.head_dim, pb.S, pb.m, pb.P, pb.scale, csr, dq_part, dk, dv);
+            pb.n_blocks, pb.n_heads, pb.n_kv_heads, pb.head_dim, pb.S, pb.m, pb.P, pb.scale, csr, dq_part, dk, dv);
     } else {
         auto kern = attn_bwd_simt_kernel<float>;
         SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         kern<<<simt_grid(pb), kThreads, smem, c.stream>>>(
             static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
-            static_cast<const float*>(dO), lse, D, pb.s, pb.a, pb.B, pb.n_blocks, pb.n_heads, pb.head_dim, pb.S, pb.m,
+            static_cast<const float*>(dO), lse, D, pb.s, pb.a, pb.B, pb.n_blocks, pb.n_heads, pb.n_kv_heads, pb.head_dim, pb.S, pb.m,
             pb.P, pb.scale, csr, dq_part, dk, dv);
     }
     SKV_LAUNCHED();

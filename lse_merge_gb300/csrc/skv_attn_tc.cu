@@ -64,13 +64,14 @@ template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_v, const int32_t* __restrict__ s,
-                   const int32_t* __restrict__ a, int B, int64_t Qn, int H, int64_t S, int m,
+                   const int32_t* __restrict__ a, int B, int64_t Qn, int H, int gq, int64_t S, int m,
                    float scale_log2, skv::RankCSR csr, const int4* __restrict__ qtb, int n_qt,
                    float* __restrict__ o_part, float* __restrict__ lse_part, int* status, long long wait_limit) {
     extern __shared__ unsigned char smem_raw[];
     FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qt0 = 2 * blockIdx.x, h = blockIdx.y, p = blockIdx.z;
+    const int kvh = h / gq;                          // key/value head of this query head
     constexpr int NP = D / 64;                       // 64-column panels per row
     constexpr uint32_t kTileBytes = BN * D * 2;      // one K or V tile (== Q tile)
 
@@ -297,10 +298,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                     if (*(volatile int*)&sm.abort_flag) break;
                     mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
                     for (int c = 0; c < NP; ++c)
-                        tma_load_2d(sm.k[st][c], &map_k, &sm.k_full[st], h * D + c * 64, (int)x0);
+                        tma_load_2d(sm.k[st][c], &map_k, &sm.k_full[st], kvh * D + c * 64, (int)x0);
                     mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
                     for (int c = 0; c < NP; ++c)
-                        tma_load_2d(sm.v[st][c], &map_v, &sm.v_full[st], h * D + c * 64, (int)x0);
+                        tma_load_2d(sm.v[st][c], &map_v, &sm.v_full[st], kvh * D + c * 64, (int)x0);
                     ++n;
                 }
                 // every load this thread issued has landed before the block exits
@@ -395,8 +396,8 @@ skv_status launch_fwd(const skv_problem& pb, const void* q, const void* k, const
                       float* o_part, float* lse_part, void* scratch, const skv_host::Ctx& c) {
     const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, Qn, int64_t(pb.n_heads) * D) || !make_map(&mk, k, pb.S, int64_t(pb.n_heads) * D) ||
-        !make_map(&mv, v, pb.S, int64_t(pb.n_heads) * D))
+    if (!make_map(&mq, q, Qn, int64_t(pb.n_heads) * D) || !make_map(&mk, k, pb.S, int64_t(pb.n_kv_heads) * D) ||
+        !make_map(&mv, v, pb.S, int64_t(pb.n_kv_heads) * D))
         return SKV_ERR_CUDA;
     size_t smem = sizeof(FwdSmem<D>) + 1024;
     if (smem < 120 * 1024) smem = 120 * 1024;   // one block per SM: it owns all 512 TMEM columns
@@ -414,7 +415,8 @@ skv_status launch_fwd(const skv_problem& pb, const void* q, const void* k, const
     const dim3 grid((unsigned)((n_qt + 1) / 2), (unsigned)pb.n_heads, (unsigned)pb.P);
     const float scale_log2 = pb.scale * 1.4426950408889634f;
     skv_host::timer_begin(skv_host::kTimeFwd, c.stream);
-    kern<<<grid, kFwdThreads, smem, c.stream>>>(mq, mk, mv, pb.s, pb.a, pb.B, Qn, pb.n_heads, pb.S, pb.m, scale_log2,
+    kern<<<grid, kFwdThreads, smem, c.stream>>>(mq, mk, mv, pb.s, pb.a, pb.B, Qn, pb.n_heads,
+                                                pb.n_heads / pb.n_kv_heads, pb.S, pb.m, scale_log2,
                                                 csr, qtb, (int)n_qt, o_part, lse_part, c.status, c.wait_limit);
     skv_host::timer_end(skv_host::kTimeFwd, c.stream);
     SKV_LAUNCHED();

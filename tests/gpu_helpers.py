@@ -17,7 +17,7 @@ def dev_inputs(w: Workload, with_grad=None):
     d = {"s": inp.s.cuda(), "a": inp.a.cuda(), "q": inp.q.cuda(), "k": inp.k.cuda(), "v": inp.v.cuda(),
          "dO": inp.dO.cuda() if inp.dO is not None else None}
     tdt = torch.float32 if w.dtype == "fp32" else torch.bfloat16
-    prob = skv.Problem(d["s"], d["a"], w.B, w.H, w.d, w.S, w.m, w.P, tdt)
+    prob = skv.Problem(d["s"], d["a"], w.B, w.H, w.d, w.S, w.m, w.P, tdt, n_kv_heads=w.Hkv)
     return inp, d, prob
 
 

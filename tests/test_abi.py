@@ -39,16 +39,17 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_struct_layout():
-    # int32 x4, int64, int32 x3, (pad), 2 pointers, enum, float
-    assert ctypes.sizeof(_lib.SkvProblem) == 64
+    # int32 x4, int64, int32 x3, (pad), 2 pointers, enum, float, int32, (pad)
+    assert ctypes.sizeof(_lib.SkvProblem) == 72
     assert _lib.SkvProblem.S.offset == 16
     assert _lib.SkvProblem.s.offset == 40
     assert _lib.SkvProblem.dtype.offset == 56
+    assert _lib.SkvProblem.n_kv_heads.offset == 64
 
 
 def prob(**kw):
     base = dict(B=16, n_blocks=8, n_heads=4, head_dim=64, S=2048, m=512, P=4, J=1, s=0x1000, a=0x2000,
-                dtype=0, scale=0.0)
+                dtype=0, scale=0.0, n_kv_heads=0)
     base.update(kw)
     return _lib.SkvProblem(*[base[f] for f, _ in _lib.SkvProblem._fields_])
 
@@ -97,6 +98,21 @@ def test_host_validation_rejects_before_launch(lib):
                             None) == E.SKV_ERR_INVALID_ARG
     assert lib.skv_attn_fwd(ctypes.byref(prob(head_dim=32)), None, None, None, None, None, None, None, 0,
                             None) == E.SKV_ERR_UNSUPPORTED
+    # grouped-query layouts: Hkv must divide H (0 selects H)
+    for hkv in (-1, 3, 5, 8):
+        assert lib.skv_chunk_costs(ctypes.byref(prob(n_kv_heads=hkv)), ctypes.c_void_p(0x1000),
+                                   None) == E.SKV_ERR_INVALID_ARG
+    for hkv in (1, 2, 4):
+        assert lib.skv_attn_fwd(ctypes.byref(prob(dtype=1, n_kv_heads=hkv)), None, None, None, None, None, None,
+                                ctypes.c_void_p(0x1000), 0, None) == E.SKV_ERR_WORKSPACE
+    # merge backward: the same argument checks as the merge
+    assert lib.skv_lse_merge_bwd(ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1000), 0, 10, 64, ctypes.c_void_p(0x1000),
+                                 0, None, None, ctypes.c_void_p(0x1000), None) == E.SKV_ERR_INVALID_ARG
+    assert lib.skv_lse_merge_bwd(ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1000), 2, 10, 96, ctypes.c_void_p(0x1000),
+                                 0, None, None, ctypes.c_void_p(0x1000), None) == E.SKV_ERR_UNSUPPORTED
+    assert lib.skv_lse_merge_bwd(ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1000), 2, 10, 64, ctypes.c_void_p(0x1000),
+                                 0, None, None, None, None) == E.SKV_ERR_INVALID_ARG
+    assert lib.skv_lse_merge_bwd(None, None, 2, 0, 64, None, 0, None, None, None, None) == E.SKV_OK
     assert lib.skv_set_wait_limit(5) == E.SKV_OK
     assert lib.skv_set_wait_limit(0) == E.SKV_OK
 

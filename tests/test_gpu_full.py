@@ -9,11 +9,11 @@ import torch
 import lse_merge_gb300 as skv
 import oracle as orc
 from gpu_helpers import TOL_BF16, TOL_BF16_LSE, assert_lse_equal, maxabs
-from workloads import LONG_1M, PACKED, make_inputs, qs_sweep
+from workloads import LONG_1M, PACKED, PACKED_KV8, make_inputs, qs_sweep
 
 pytestmark = pytest.mark.gpu
 
-FULL = [PACKED, LONG_1M, qs_sweep(4, "contiguous"), qs_sweep(32, "lpt")]
+FULL = [PACKED, LONG_1M, qs_sweep(4, "contiguous"), qs_sweep(32, "lpt"), PACKED_KV8]
 
 
 def sample_blocks(N, seed):
@@ -40,7 +40,7 @@ def full_run(request):
     w = request.param
     inp = make_inputs(w, device="cuda")
     s, a = inp.s.cuda(), inp.a.cuda()
-    prob = skv.Problem(s, a, w.B, w.H, w.d, w.S, w.m, w.P, torch.bfloat16)
+    prob = skv.Problem(s, a, w.B, w.H, w.d, w.S, w.m, w.P, torch.bfloat16, n_kv_heads=w.Hkv)
     costs, roc, _, _ = skv.plan(prob, w.order)
     o_part, lse_part = skv.attn_fwd(prob, inp.q, inp.k, inp.v, roc)
     o, lse = skv.lse_merge(o_part, lse_part, out_dtype=torch.bfloat16)
@@ -120,7 +120,7 @@ def test_full_dq_sampled_blocks(full_run):
 
 def test_full_dkdv_sampled_keys(full_run):
     w, inp, prob, _, _, _, _, _, dq, dk, dv = full_run
-    heads = [0, w.H - 1]
+    heads = [0, w.KVH - 1]                    # key/value heads (each sums its query heads)
     keys = [k for k in few_attender_keys(inp.s, inp.a) if k < w.S]
     r_dk, r_dv = orc.backward_key_rows(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, inp.dO, keys, heads)
     kt = torch.as_tensor(keys, device="cuda")
@@ -139,9 +139,12 @@ def test_full_gradient_properties(full_run):
     unseen = (~seen).nonzero().flatten().cuda()
     if unseen.numel():
         assert float(dk[unseen].abs().max()) == 0.0 and float(dv[unseen].abs().max()) == 0.0
-    # softmax rows sum to one: sum_x dv_x = sum_r dO_r (every row sees some key here)
-    for h in (0, w.H - 1):
-        lhs = dv[:, h].double().sum(0)
-        rhs = inp.dO[:, h].double().sum(0)
-        scale = inp.dO[:, h].double().abs().sum(0)
+    # softmax rows sum to one: sum_x dv_x = sum_r dO_r over the key/value head's
+    # query heads (every row sees some key here)
+    g = w.H // w.KVH
+    for c in (0, w.KVH - 1):
+        lhs = dv[:, c].double().sum(0)
+        grp = inp.dO[:, c * g:(c + 1) * g].double()
+        rhs = grp.sum((0, 1))
+        scale = grp.abs().sum((0, 1))
         assert float(((lhs - rhs).abs() / scale).max()) < 1e-2

@@ -46,6 +46,11 @@ class Workload:
     do_std: float           # dO ~ N(0,1) * do_std
     order: str              # "contiguous" or "lpt"
     backward: bool          # whether the workload runs the backward pass
+    Hkv: int = 0            # key/value heads (grouped queries); 0 means H
+
+    @property
+    def KVH(self) -> int:
+        return self.Hkv or self.H
 
     @property
     def S(self) -> int:
@@ -102,7 +107,12 @@ def qs_sweep(ratio: int, order: str = "lpt") -> Workload:
 PROFILE_SMALL = Workload("profile_1x128k", 6, 1, 131072, 512, *_resp(131072), 16, 8, 128, 4096, 8,
                          "bf16", 0.5, 1.0, "lpt", True)
 
-WORKLOADS = {w.name: w for w in (TINY_FP32, BF16_FWD, PACKED, LONG_1M, PROFILE_SMALL)}
+# Grouped-query layouts of the paper's drafters (Table 2: 32 query heads over 8
+# or 4 key/value heads, head dim 128) on the packed shape.
+PACKED_KV8 = PACKED.with_(name="packed_4x128k_kv8", Hkv=8)
+PACKED_KV4 = PACKED.with_(name="packed_4x128k_kv4", Hkv=4)
+
+WORKLOADS = {w.name: w for w in (TINY_FP32, BF16_FWD, PACKED, LONG_1M, PROFILE_SMALL, PACKED_KV8, PACKED_KV4)}
 for _r in (4, 8, 16, 32):
     for _o in ("lpt", "contiguous"):
         _w = qs_sweep(_r, _o)
@@ -131,8 +141,8 @@ class Inputs:
     s: torch.Tensor          # int32 [N]
     a: torch.Tensor          # int32 [N]
     q: torch.Tensor          # [Q, H, d] fp32 or bf16 (exactly what the GPU receives)
-    k: torch.Tensor          # [S, H, d]
-    v: torch.Tensor          # [S, H, d]
+    k: torch.Tensor          # [S, Hkv, d]
+    v: torch.Tensor          # [S, Hkv, d]
     dO: Optional[torch.Tensor]  # [Q, H, d] or None
 
 
@@ -165,22 +175,22 @@ def make_inputs(w: Workload, with_grad: Optional[bool] = None, pin: bool = False
         return out.pin_memory() if (pin and device == "cpu") else out
 
     q = draw((w.Q, w.H, w.d), w.qkv_std)
-    k = draw((w.S, w.H, w.d), w.qkv_std)
-    v = draw((w.S, w.H, w.d), w.qkv_std)
+    k = draw((w.S, w.KVH, w.d), w.qkv_std)
+    v = draw((w.S, w.KVH, w.d), w.qkv_std)
     want = w.backward if with_grad is None else with_grad
     dO = draw((w.Q, w.H, w.d), w.do_std) if want else None
     return Inputs(w, s, a, q, k, v, dO)
 
 
 def block_kv(w: Workload, device: str = "cpu"):
-    """(k_blk, v_blk) [Q, H, d]: the block tokens' own keys and values for the
+    """(k_blk, v_blk) [Q, Hkv, d]: the block tokens' own keys and values for the
     block-local term, drawn like q from their own seeded generator."""
     tdt = torch.float32 if w.dtype == "fp32" else torch.bfloat16
     g = torch.Generator(device=device)
     g.manual_seed(w.seed + 1000003)
     out = []
     for _ in range(2):
-        x = torch.empty(w.Q, w.H, w.d, dtype=tdt, device=device)
+        x = torch.empty(w.Q, w.KVH, w.d, dtype=tdt, device=device)
         flat = x.view(-1)
         step = 1 << 26
         for i in range(0, flat.numel(), step):
