@@ -66,7 +66,10 @@ __device__ __forceinline__ void stage_rows(const T* src, int i, int B, int H, in
 
 // shared floats of one CTA
 __host__ __device__ inline int fwd_floats(int B, int d) { return 2 * B * (d + 1) + B * d + B * 32; }
-__host__ __device__ inline int bwd_floats(int B, int d) { return 6 * B * (d + 1) + 2 * B * 32 + 32; }
+// (the group's dk/dv accumulators, 2 B (d + 1) more, only with grouped queries)
+__host__ __device__ inline int bwd_floats(int B, int d, bool grouped) {
+    return (grouped ? 6 : 4) * B * (d + 1) + 2 * B * 32 + 32;
+}
 
 // One CTA per (block i, head h).  Phase 1: warp w takes rows r = w, w + 4, ...;
 // lane j < B scores key j (a d-long dot product), the row's softmax runs across
@@ -140,10 +143,11 @@ block_local_bwd_kernel(const T* __restrict__ q, const T* __restrict__ kb, const 
     float* sav = sak + B * dp;   // [B][d + 1] dv_blk rows
     stage_rows(kb, i, B, Hkv, kvh, d, sk, dp);
     stage_rows(vb, i, B, Hkv, kvh, d, sv, dp);
-    for (int e = threadIdx.x; e < B * dp; e += blockDim.x) {
-        sak[e] = 0.f;
-        sav[e] = 0.f;
-    }
+    if (gq > 1)
+        for (int e = threadIdx.x; e < B * dp; e += blockDim.x) {
+            sak[e] = 0.f;
+            sav[e] = 0.f;
+        }
     const float scale_log2 = scale * kLog2e;
     for (int h = kvh * gq; h < (kvh + 1) * gq; ++h) {
         __syncthreads();   // the previous query head is done with sq, sg, sp, ss
@@ -192,24 +196,32 @@ block_local_bwd_kernel(const T* __restrict__ q, const T* __restrict__ kb, const 
                 dst[t] = fmaf(scale, acc, dst[t]);
             }
         }
-        for (int j = warp; j < B; j += kWarps)     // dk, dv parts of the block keys (thread-owned)
+        for (int j = warp; j < B; j += kWarps) {   // dk, dv parts of the block keys (thread-owned)
+            const int64_t g0 = ((int64_t(i) * B + j) * Hkv + kvh) * d;
             for (int t = lane; t < d; t += 32) {
                 float ak = 0.f, av = 0.f;
                 for (int r = 0; r < B; ++r) {
                     ak = fmaf(ss[r * 32 + j], sq[r * dp + t], ak);
                     av = fmaf(sp[r * 32 + j], sg[r * dp + t], av);
                 }
-                sak[j * dp + t] = fmaf(scale, ak, sak[j * dp + t]);
-                sav[j * dp + t] += av;
+                if (gq == 1) {                        // one query head: straight out
+                    dkb[g0 + t] = scale * ak;
+                    dvb[g0 + t] = av;
+                } else {
+                    sak[j * dp + t] = fmaf(scale, ak, sak[j * dp + t]);
+                    sav[j * dp + t] += av;
+                }
             }
-    }
-    for (int j = warp; j < B; j += kWarps) {       // the same threads wrote these: no barrier
-        const int64_t g0 = ((int64_t(i) * B + j) * Hkv + kvh) * d;
-        for (int t = lane; t < d; t += 32) {
-            dkb[g0 + t] = sak[j * dp + t];
-            dvb[g0 + t] = sav[j * dp + t];
         }
     }
+    if (gq > 1)
+        for (int j = warp; j < B; j += kWarps) {   // the same threads wrote these: no barrier
+            const int64_t g0 = ((int64_t(i) * B + j) * Hkv + kvh) * d;
+            for (int t = lane; t < d; t += 32) {
+                dkb[g0 + t] = sak[j * dp + t];
+                dvb[g0 + t] = sav[j * dp + t];
+            }
+        }
 }
 
 }  // namespace
@@ -217,7 +229,7 @@ block_local_bwd_kernel(const T* __restrict__ q, const T* __restrict__ kb, const 
 namespace skv_internal {
 
 bool block_local_supported(const skv_problem& pb) {
-    return pb.B <= 32 && size_t(bwd_floats(pb.B, pb.head_dim)) * 4 <= 200 * 1024;
+    return pb.B <= 32 && size_t(bwd_floats(pb.B, pb.head_dim, pb.n_kv_heads < pb.n_heads)) * 4 <= 200 * 1024;
 }
 
 skv_status launch_block_local_fwd(const skv_problem& pb, const void* q, const void* kb, const void* vb, float* o,
@@ -255,7 +267,7 @@ skv_status launch_block_local_bwd(const skv_problem& pb, const void* q, const vo
     const int64_t items = int64_t(N) * Hkv;        // (block, key/value head)
     if (items == 0) return SKV_OK;
     if (items > 0x7fffffffLL) return SKV_ERR_UNSUPPORTED;
-    const int smem = bwd_floats(B, d) * 4;
+    const int smem = bwd_floats(B, d, Hkv < H) * 4;
     skv_host::timer_begin(skv_host::kTimeLocalBwd, c.stream);
     if (pb.dtype == SKV_BF16) {
         using T = __nv_bfloat16;
