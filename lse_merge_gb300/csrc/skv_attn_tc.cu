@@ -63,7 +63,8 @@ struct __align__(1024) FwdSmem {
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                   const __grid_constant__ CUtensorMap map_v, const int32_t* __restrict__ s,
+                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                   const int32_t* __restrict__ s,
                    const int32_t* __restrict__ a, int B, int64_t Qn, int H, int gq, int64_t S, int m,
                    float scale_log2, skv::RankCSR csr, const int4* __restrict__ qtb, int n_qt,
                    float* __restrict__ o_part, float* __restrict__ lse_part, int* status, long long wait_limit) {
@@ -248,24 +249,40 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         if (ok && !aborted && (n == 0 || uniform_wait(&sm.mma_fin, 0))) {
             const bool mine = live && l > 0.f;
             const float inv = mine ? 1.f / l : 0.f;
-            float* dst = o_part + ((int64_t(p) * Qn + row) * H + h) * D;
             if (n > 0 && __any_sync(kAll, mine)) {
+                // o_j rows leave through the (now idle) K/V ring: each warp stages its 32 rows
+                // as 128-byte-swizzled 32 x 32 fp32 boxes (16-byte chunk u of row r at chunk
+                // u ^ (r % 8)) and writes them with TMA stores; rows past Qn are dropped.
+                // Rows that see no key are written as zeros (their lse_part is -inf).
                 tc_fence_after();
+                unsigned char* stage = reinterpret_cast<unsigned char*>(&sm.k[0][0][0]) + j * (D / 32) * (BM * 128);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t rr[32];
                     tmem_ld32(tO + lane_base + c * 32, rr);
                     tmem_ld_wait();
-                    if (mine) {
+                    unsigned char* panel = stage + c * (BM * 128) + r * 128;
 #pragma unroll
-                        for (int jj = 0; jj < 32; jj += 4) {
-                            float4 v4 = make_float4(__uint_as_float(rr[jj]) * inv, __uint_as_float(rr[jj + 1]) * inv,
-                                                    __uint_as_float(rr[jj + 2]) * inv,
-                                                    __uint_as_float(rr[jj + 3]) * inv);
-                            __stcs(reinterpret_cast<float4*>(dst + c * 32 + jj), v4);
-                        }
+                    for (int u = 0; u < 8; ++u) {
+                        const float4 v4 = mine ? make_float4(__uint_as_float(rr[4 * u]) * inv,
+                                                             __uint_as_float(rr[4 * u + 1]) * inv,
+                                                             __uint_as_float(rr[4 * u + 2]) * inv,
+                                                             __uint_as_float(rr[4 * u + 3]) * inv)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                        *reinterpret_cast<float4*>(panel + ((u ^ (r & 7)) * 16)) = v4;
                     }
                 }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c)
+                        tma_store_3d(&map_o, stage + c * (BM * 128) + quad * 32 * 128, h * D + c * 32,
+                                     (qt0 + j) * BM + quad * 32, p);
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                }
+                __syncwarp();
             }
             if (live)
                 lse_part[(int64_t(p) * Qn + row) * H + h] =
@@ -395,9 +412,10 @@ template <int D>
 skv_status launch_fwd(const skv_problem& pb, const void* q, const void* k, const void* v, skv::RankCSR csr,
                       float* o_part, float* lse_part, void* scratch, const skv_host::Ctx& c) {
     const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, q, Qn, int64_t(pb.n_heads) * D) || !make_map(&mk, k, pb.S, int64_t(pb.n_kv_heads) * D) ||
-        !make_map(&mv, v, pb.S, int64_t(pb.n_kv_heads) * D))
+        !make_map(&mv, v, pb.S, int64_t(pb.n_kv_heads) * D) ||
+        !make_map_f32_3d(&mo, o_part, pb.P, Qn, int64_t(pb.n_heads) * D))
         return SKV_ERR_CUDA;
     size_t smem = sizeof(FwdSmem<D>) + 1024;
     if (smem < 120 * 1024) smem = 120 * 1024;   // one block per SM: it owns all 512 TMEM columns
@@ -415,7 +433,7 @@ skv_status launch_fwd(const skv_problem& pb, const void* q, const void* k, const
     const dim3 grid((unsigned)((n_qt + 1) / 2), (unsigned)pb.n_heads, (unsigned)pb.P);
     const float scale_log2 = pb.scale * 1.4426950408889634f;
     skv_host::timer_begin(skv_host::kTimeFwd, c.stream);
-    kern<<<grid, kFwdThreads, smem, c.stream>>>(mq, mk, mv, pb.s, pb.a, pb.B, Qn, pb.n_heads,
+    kern<<<grid, kFwdThreads, smem, c.stream>>>(mq, mk, mv, mo, pb.s, pb.a, pb.B, Qn, pb.n_heads,
                                                 pb.n_heads / pb.n_kv_heads, pb.S, pb.m, scale_log2,
                                                 csr, qtb, (int)n_qt, o_part, lse_part, c.status, c.wait_limit);
     skv_host::timer_end(skv_host::kTimeFwd, c.stream);
@@ -429,7 +447,8 @@ namespace skv_tc {
 
 bool fwd_supported(const skv_problem& pb) {
     return pb.dtype == SKV_BF16 && (pb.head_dim == 64 || pb.head_dim == 128) && pb.m % BN == 0 &&
-           pb.P <= 65535 && pb.n_heads <= 65535 && pb.S <= INT32_MAX;
+           pb.P <= 65535 && pb.n_heads <= 65535 && pb.S <= INT32_MAX &&
+           int64_t(pb.n_blocks) * pb.B <= INT32_MAX;
 }
 size_t fwd_scratch_bytes(const skv_problem& pb) {   // per query tile key bounds (int4)
     const int64_t Qn = int64_t(pb.n_blocks) * pb.B;

@@ -128,5 +128,18 @@ inline bool make_map_f32(CUtensorMap* map, void* ptr, int64_t rows, int64_t cols
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+// 3D fp32 view [d2][d1][cols] of a row-major tensor, 32x32x1 boxes, 128-byte
+// swizzle: rows past d1 inside one d2 slice are dropped by a store.
+inline bool make_map_f32_3d(CUtensorMap* map, void* ptr, int64_t d2, int64_t d1, int64_t cols) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)d1, (cuuint64_t)d2};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)(cols * d1) * 4};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace skv_tcc
