@@ -64,6 +64,30 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+# Multi-rank rules of the measurement (weak scaling: one independent replica
+# per rank, no collective on the data path).
+
+def replica(w, rank: int):
+    """Rank r's replica: the same workload shape with its own seed."""
+    return w.with_(seed=w.seed + 1000 * rank) if rank else w
+
+
+def slowest(values, world: int, device):
+    """Per-rank times -> the slowest rank's (the job ends with its last replica)."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_tflops(flop_per_rank_step: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the work of every rank over the slowest rank's time."""
+    return flop_per_rank_step * world / (ms * 1e-3) / 1e12
+
+
 class ClockSampler:
     """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -276,8 +300,7 @@ def run_ours(args):
 
     lib = _lib.load()
     w = WORKLOADS[args.workload]
-    if world > 1:
-        w = w.with_(seed=w.seed + 1000 * rank)     # independent replica per rank
+    w = replica(w, rank)                           # independent replica per rank
     dev = torch.device("cuda", local_rank)
     inp = make_inputs(w, with_grad=w.backward, device=str(dev))
     tdt = torch.float32 if w.dtype == "fp32" else torch.bfloat16
@@ -365,10 +388,7 @@ def run_ours(args):
         ph["merge"].append(e[2].elapsed_time(e[3]))
         ph["bwd"].append(e[3].elapsed_time(e[4]))
     ph = {kk: statistics.mean(vv) for kk, vv in ph.items()}
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = slowest([ms], world, dev)[0]
     if skv.stream_status() != 0:
         raise RuntimeError("device status set during the timed region")
     # per-kernel durations: the library's own CUDA events on the launching
@@ -432,7 +452,7 @@ def run_ours(args):
     fwd_flops = 4.0 * d * pairs
     bwd_flops = 8.0 * d * pairs if w.backward else 0.0
     step_flops = fwd_flops + bwd_flops
-    value = step_flops * world / (ms * 1e-3) / 1e12
+    value = job_tflops(step_flops, world, ms)
     pk, pk_kind = peaks()
     sustained = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -574,16 +594,12 @@ def run_ours(args):
             raise RuntimeError("device status set during the end-to-end pass")
         e_ms = t_s.elapsed_time(t_e) / kp
         del sets
-        if world > 1:
-            tt = torch.tensor([e_ms, serial_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms, serial_ms = float(tt[0].item()), float(tt[1].item())
-        e2e = {"value": step_flops * world / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+        e_ms, serial_ms = slowest([e_ms, serial_ms], world, dev)
+        e2e = {"value": job_tflops(step_flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "mode": f"pipelined over {kp} steps: step t+1's inputs up and step t's results down "
                        "on two copy streams while step t computes (two device buffer sets)",
-               "serial": {"ms_per_step": serial_ms,
-                          "value": step_flops * world / (serial_ms * 1e-3) / 1e12}}
+               "serial": {"ms_per_step": serial_ms, "value": job_tflops(step_flops, world, serial_ms)}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -1,0 +1,60 @@
+"""The multi-rank rules of bench.py, on CPU with two gloo ranks (127.0.0.1):
+every rank runs its own replica (its own seed, same shape), the reported time
+is the slowest rank's, and the job's throughput counts the work of every rank
+over that time (weak scaling, no collective on the data path)."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from workloads import PACKED
+
+
+def _free_port():
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mine = [10.0 + 5.0 * rank, 3.0 - rank]        # rank 1 is slower on the first, faster on the second
+        got = bench.slowest(mine, world, "cpu")
+        dist.barrier()
+        q.put((rank, got, bench.replica(PACKED, rank).seed))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_time():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = {}
+    for _ in range(world):
+        rank, got, seed = q.get(timeout=120)
+        res[rank] = (got, seed)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank in range(world):
+        assert res[rank][0] == [15.0, 3.0]           # the maximum of each entry over ranks
+    assert res[0][1] == PACKED.seed and res[1][1] != res[0][1]
+
+
+def test_single_rank_and_job_throughput():
+    assert bench.slowest([4.0, 2.0], 1, "cpu") == [4.0, 2.0]
+    assert bench.replica(PACKED, 0) is PACKED
+    r3 = bench.replica(PACKED, 3)
+    assert (r3.S, r3.Q, r3.H, r3.d, r3.P) == (PACKED.S, PACKED.Q, PACKED.H, PACKED.d, PACKED.P)
+    # 2 TFLOP per rank-step, 4 ranks, 10 ms for the slowest: 800 TFLOP/s for the job
+    assert bench.job_tflops(2e12, 4, 10.0) == pytest.approx(800.0)
