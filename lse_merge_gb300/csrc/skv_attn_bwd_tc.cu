@@ -607,7 +607,9 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_co
     QTiles<D>& tl = sm.t;
     QBars& bb = sm.b;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qt = blockIdx.x, h = blockIdx.y;
+    // query tiles in descending order: the last tiles of a sample see the longest
+    // windows, so the longest blocks start first and the grid's tail is short ones
+    const int qt = gridDim.x - 1 - blockIdx.x, h = blockIdx.y;
     const int kvh = h / gq;                          // key/value head of this query head
     constexpr int NP = D / 64;
     constexpr uint32_t kTile = BM * D * 2;

@@ -71,7 +71,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     extern __shared__ unsigned char smem_raw[];
     FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qt0 = 2 * blockIdx.x, h = blockIdx.y, p = blockIdx.z;
+    // query tile pairs in descending order: the last tiles of a sample see the longest
+    // windows, so the longest blocks start first and each head's tail is short ones
+    const int qt0 = 2 * (gridDim.x - 1 - blockIdx.x), h = blockIdx.y, p = blockIdx.z;
     const int kvh = h / gq;                          // key/value head of this query head
     constexpr int NP = D / 64;                       // 64-column panels per row
     constexpr uint32_t kTileBytes = BN * D * 2;      // one K or V tile (== Q tile)
