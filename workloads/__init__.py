@@ -81,8 +81,8 @@ def _resp(L: int):
     return L // 4, L
 
 
-# The five workloads.  Sizes follow the task's configuration list; the
-# distributions the list leaves open are read as in the design doc.
+# The five evaluation workloads (sizes of the paper's step-time studies, §5):
+# q, k, v ~ N(0, 1) * qkv_std and dO ~ N(0, 1) * do_std, as listed below.
 TINY_FP32 = Workload("tiny_fp32", 1, 1, 2048, 8, 256, 2049, 16, 4, 64, 512, 4,
                      "fp32", 1.0, 1.0, "contiguous", True)
 BF16_FWD = Workload("bf16_fwd", 2, 1, 32768, 64, *_resp(32768), 16, 16, 128, 4096, 8,
