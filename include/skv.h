@@ -26,7 +26,8 @@
  *    skv_stream_status.  Kernels clamp every index they derive from anchors,
  *    so bad metadata yields wrong numbers, never an out-of-bounds access.
  *  - Layouts are row-major.  Query tensors are [Q][H][d] (Q = n_blocks * B),
- *    context tensors [S][H][d]; query row r belongs to block floor(r / B).
+ *    context tensors [S][Hkv][d] (Hkv = H without grouped queries); query row r
+ *    belongs to block floor(r / B).
  */
 #ifndef SKV_H_
 #define SKV_H_
@@ -66,8 +67,7 @@ typedef enum skv_dtype {
  * [j*m, (j+1)*m); P virtual ranks hold J chunks each (P*J*m == S).
  * With grouped-query attention (the drafters of Table 2: 32 query heads over
  * 4 or 8 key/value heads) k, v, dk, dv and the block-local k_blk, v_blk,
- * dk_blk, dv_blk have Hkv heads in place of H; every shape below written with
- * [H] for those tensors means [Hkv].
+ * dk_blk, dv_blk have Hkv heads in place of H.
  */
 typedef struct skv_problem {
     int32_t B;            /* block size: query rows per anchor, 1..128        */
@@ -153,7 +153,7 @@ SKV_API size_t skv_workspace_bytes(const skv_problem* prob, int which);
  * K_p get lse_part = -inf; their o_part row is unspecified (never read by
  * skv_lse_merge).
  *   q             device [Q][H][d], dtype prob->dtype
- *   k, v          device [S][H][d], dtype prob->dtype; rows 16-byte aligned
+ *   k, v          device [S][Hkv][d], dtype prob->dtype; rows 16-byte aligned
  *   rank_of_chunk device int32[S/m]
  *   o_part        device float[P][Q][H][d], written
  *   lse_part      device float[P][Q][H], written
@@ -243,11 +243,12 @@ SKV_API skv_status skv_lse_merge_bwd(const float* o_part, const float* lse_part,
  * P_rx (dO_r . v_x - D_r) with P_rx = exp(z_rx - lse_r), which equals the
  * per-rank route exactly.
  *   q, dO     device [Q][H][d], dtype prob->dtype
- *   k, v      device [S][H][d], dtype prob->dtype
+ *   k, v      device [S][Hkv][d], dtype prob->dtype
  *   o         device [Q][H][d], dtype prob->dtype (the merged output)
  *   lse       device float[Q][H] (the merged log-sum-exp, natural log)
  *   dq        device float[Q][H][d], written
- *   dk, dv    device float[S][H][d], written (keys no query sees get 0)
+ *   dk, dv    device float[S][Hkv][d], written (keys no query sees get 0; a
+ *             key/value head sums the gradients of its query heads)
  *   workspace device, >= skv_workspace_bytes(prob, 1) bytes
  */
 SKV_API skv_status skv_attn_bwd(const skv_problem* prob, const void* q, const void* k, const void* v,
@@ -263,7 +264,8 @@ SKV_API skv_status skv_attn_bwd(const skv_problem* prob, const void* q, const vo
  * context chunk, so its result is one more partial of Eq. 4: write it after
  * the P rank partials (o_loc = o_part + P*Q*H*d, lse_loc = lse_part + P*Q*H)
  * and merge P + 1 partials with skv_lse_merge to get the whole mask.
- *   q, k_blk, v_blk  device [Q][H][d], dtype prob->dtype (Q = n_blocks * B)
+ *   q                device [Q][H][d], dtype prob->dtype (Q = n_blocks * B)
+ *   k_blk, v_blk     device [Q][Hkv][d], dtype prob->dtype
  *   o_loc            device float[Q][H][d], written
  *   lse_loc          device float[Q][H], written (natural log)
  * prob->B <= 32 and head_dim 64 or 128, else SKV_ERR_UNSUPPORTED; the anchor
@@ -281,7 +283,8 @@ SKV_API skv_status skv_block_local_fwd(const skv_problem* prob, const void* q, c
  *   dq               device float[Q][H][d], ACCUMULATED: call after
  *                    skv_attn_bwd (which writes the context part) on the same
  *                    stream, and dq holds the whole-mask gradient
- *   dk_blk, dv_blk   device float[Q][H][d], written
+ *   dk_blk, dv_blk   device float[Q][Hkv][d], written (summed over each key/value
+ *                    head's query heads)
  */
 SKV_API skv_status skv_block_local_bwd(const skv_problem* prob, const void* q, const void* k_blk, const void* v_blk,
                                        const void* o, const float* lse, const void* dO, float* dq, float* dk_blk,
