@@ -9,7 +9,8 @@ Drafters" (Zhang, Zhang, Xie, Fan, You), cited below as [Split-KV ...].
 Notation (paper's): B block size, N blocks, Q = N*B query rows, S packed
 context, H heads, d head dim, m chunk length, P ranks, J chunks per rank,
 anchor metadata A = {(s_i, a_i)}.  Query row r belongs to block floor(r/B).
-Tensors: q, dO [Q, H, d]; k, v [S, H, d]; outputs o [Q, H, d], lse [Q, H].
+Tensors: q, dO [Q, H, d]; k, v [S, Hkv, d] (Hkv = H, or fewer key/value heads
+in a grouped-query layout, see kv_head); outputs o [Q, H, d], lse [Q, H].
 
 Everything here is written as the definition reads: the mask is materialised
 as an explicit boolean row over all S context keys, the softmax is the
@@ -349,7 +350,7 @@ def attention_backward(q, k, v, s, a, B: int, dO, scale: Optional[float] = None,
     Split-KV computes the same gradients per rank (Alg. 1 lines 12-21) and sums
     dq over ranks; the partitioned route is ``partitioned_backward``.
     ``blocks`` restricts which query blocks contribute (dk/dv then hold only
-    their contributions).  Returns (dq [Q,H,d], dk [S,H,d], dv [S,H,d])."""
+    their contributions).  Returns (dq [Q,H,d], dk [S,Hkv,d], dv [S,Hkv,d])."""
     s, a = _npi(s), _npi(a)
     N = len(s)
     Qn, H, d = q.shape
