@@ -54,6 +54,10 @@ def test_block_local_single_token_is_v():
 @pytest.mark.parametrize("w,tol,tol_l", [
     (TINY_FP32, TOL_FP32, TOL_FP32),
     (random_small(34, 2, 1536, 20, 16, 3, 128, 256, 6, dtype="bf16"), TOL_BF16, TOL_BF16_LSE),
+    # B past 16 (eight rows a warp, one lane a key): the largest block, and a ragged one
+    (random_small(35, 1, 1024, 12, 32, 3, 128, 256, 4, dtype="bf16"), TOL_BF16, TOL_BF16_LSE),
+    (random_small(36, 1, 1024, 9, 32, 2, 128, 256, 4, dtype="fp32"), TOL_FP32, TOL_FP32),
+    (random_small(37, 1, 1024, 10, 17, 2, 64, 256, 4, dtype="bf16"), TOL_BF16, TOL_BF16_LSE),
 ])
 def test_whole_mask_forward_and_backward(w, tol, tol_l):
     inp, d, prob = dev_inputs(w, with_grad=True)

@@ -38,6 +38,8 @@ def test_gqa_forward_backward(cfg):
 @pytest.mark.parametrize("w,tol,tol_l", [
     (random_small(45, 2, 1536, 20, 16, 4, 128, 256, 6, dtype="bf16").with_(Hkv=2), TOL_BF16, TOL_BF16_LSE),
     (random_small(46, 1, 512, 12, 7, 6, 64, 128, 4, dtype="fp32").with_(Hkv=2), TOL_FP32, TOL_FP32),
+    # the largest block with d = 128, four query heads on one key/value head
+    (random_small(47, 1, 1024, 10, 32, 4, 128, 256, 4, dtype="bf16").with_(Hkv=1), TOL_BF16, TOL_BF16_LSE),
 ])
 def test_gqa_whole_mask(w, tol, tol_l):
     inp, d, prob = dev_inputs(w, with_grad=True)
