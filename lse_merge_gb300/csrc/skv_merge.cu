@@ -263,14 +263,28 @@ lse_merge_bwd_kernel(const float* __restrict__ o_part, const float* __restrict__
     }
 }
 
+// CTAs of a grid-stride row kernel: as many as are resident at once on every
+// SM (one wave, so no CTA waits for a second one), capped by the warps the rows
+// need
+template <typename K>
+int one_wave(K kernel, int64_t warps_needed, const skv_host::Ctx& c) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const int64_t need = (warps_needed + kThreads / 32 - 1) / (kThreads / 32);
+    const int64_t blocks = int64_t(c.num_sms) * per_sm;
+    return (int)(blocks < need ? blocks : (need > 0 ? need : 1));
+}
+
 template <typename GT>
 skv_status merge_bwd_dispatch(const float* o_part, const float* lse_part, int P, int64_t rows, int d, const GT* dO,
                               const float* dlse, float* do_part, float* dlse_part, const skv_host::Ctx& c) {
-    int blocks = c.num_sms * 8;
-    const int64_t max_blocks = (rows + (kThreads / 32) - 1) / (kThreads / 32);
-    if (blocks > max_blocks) blocks = (int)(max_blocks > 0 ? max_blocks : 1);
-#define SKV_MB(G_, V_) \
-    lse_merge_bwd_kernel<G_, V_, GT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, dO, dlse, do_part, dlse_part)
+#define SKV_MB(G_, V_)                                                                                  \
+    {                                                                                                   \
+        auto k = lse_merge_bwd_kernel<G_, V_, GT>;                                                      \
+        k<<<one_wave(k, (rows + 32 / G_ - 1) / (32 / G_), c), kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, dO, \
+                                                                                     dlse, do_part, dlse_part); \
+    }
     switch (d) {
         case 64:  SKV_MB(16, 1); break;
         case 128: SKV_MB(32, 1); break;
@@ -289,20 +303,23 @@ skv_status merge_bwd_dispatch(const float* o_part, const float* lse_part, int P,
 template <typename OT>
 skv_status merge_dispatch(const float* o_part, const float* lse_part, int P, int64_t rows, int d, OT* o,
                           float* lse, const skv_host::Ctx& c) {
-    const int64_t warps_needed = rows;   // upper bound
-    int blocks = c.num_sms * 8;
-    const int64_t max_blocks = (warps_needed + (kThreads / 32) - 1) / (kThreads / 32);
-    if (blocks > max_blocks) blocks = (int)(max_blocks > 0 ? max_blocks : 1);
+#define SKV_M(G_, V_)                                                                                       \
+    {                                                                                                       \
+        auto k = lse_merge_kernel<G_, V_, OT>;                                                              \
+        k<<<one_wave(k, (rows + 32 / G_ - 1) / (32 / G_), c), kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, \
+                                                                                     lse);                  \
+    }
     switch (d) {
-        case 64:  lse_merge_kernel<16, 1, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
-        case 128: lse_merge_kernel<32, 1, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
-        case 256: lse_merge_kernel<32, 2, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
-        case 32:  lse_merge_kernel<8, 1, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
-        case 16:  lse_merge_kernel<4, 1, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
-        case 8:   lse_merge_kernel<2, 1, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
-        case 4:   lse_merge_kernel<1, 1, OT><<<blocks, kThreads, 0, c.stream>>>(o_part, lse_part, P, rows, o, lse); break;
+        case 64:  SKV_M(16, 1); break;
+        case 128: SKV_M(32, 1); break;
+        case 256: SKV_M(32, 2); break;
+        case 32:  SKV_M(8, 1); break;
+        case 16:  SKV_M(4, 1); break;
+        case 8:   SKV_M(2, 1); break;
+        case 4:   SKV_M(1, 1); break;
         default: return SKV_ERR_UNSUPPORTED;
     }
+#undef SKV_M
     SKV_LAUNCHED();
     return SKV_OK;
 }
