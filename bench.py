@@ -65,6 +65,16 @@ def csrc_digest():
     return h.hexdigest()
 
 
+def merge_algorithmic_bytes(lse_merged, d: int, out_b: int) -> int:
+    """HBM bytes of one merge of the partials whose l is lse_merged [P, ...]:
+    every l_p, the o_p rows with a finite l_p, and the merged o (out_b bytes an
+    element) and l per row."""
+    P = lse_merged.shape[0]
+    rows = lse_merged[0].numel()
+    finite = int(lse_merged.isfinite().sum().item())
+    return P * rows * 4 + finite * d * 4 + rows * (d * out_b + 4)
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -462,9 +472,8 @@ def run_ours(args):
     pk, pk_kind = peaks()
     sustained = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    finite = int(torch.isfinite(lse_part).sum().item())
     out_b = 2 if tdt == torch.bfloat16 else 4
-    merge_bytes = P * Q * H * 4 + finite * d * 4 + Q * H * (d * out_b + 4)
+    merge_bytes = merge_algorithmic_bytes(lse_part[:P], d, out_b)   # the P context partials the step merges
     merge_gbs = merge_bytes / (ph["merge"] * 1e-3) / 1e9
     # credited (useful) FLOP of each main kernel per launch: forward 4d per pair;
     # the backward's 8d per pair (dV, dP, dQ, dK) is credited 6d to the dK/dV

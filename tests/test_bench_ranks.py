@@ -58,3 +58,18 @@ def test_single_rank_and_job_throughput():
     assert (r3.S, r3.Q, r3.H, r3.d, r3.P) == (PACKED.S, PACKED.Q, PACKED.H, PACKED.d, PACKED.P)
     # 2 TFLOP per rank-step, 4 ranks, 10 ms for the slowest: 800 TFLOP/s for the job
     assert bench.job_tflops(2e12, 4, 10.0) == pytest.approx(800.0)
+
+
+def test_merge_bytes_match_the_oracle_count():
+    """The bench's merge bytes count the partials it is given, as the oracle's
+    count does: the block-local slot kept after the context partials is not
+    part of the context merge and must be sliced off by the caller."""
+    import numpy as np
+    import oracle as orc
+    g = torch.Generator().manual_seed(5)
+    lse = torch.randn(5, 7, 3, generator=g)
+    lse[torch.rand(5, 7, 3, generator=g) < 0.3] = float("-inf")
+    for out_b in (2, 4):
+        assert bench.merge_algorithmic_bytes(lse[:4], 16, out_b) == orc.merge_bytes(lse[:4].numpy(), 16, out_b)
+        assert bench.merge_algorithmic_bytes(lse, 16, out_b) == orc.merge_bytes(lse.numpy(), 16, out_b)
+    assert bench.merge_algorithmic_bytes(lse[:4], 16, 2) < bench.merge_algorithmic_bytes(lse, 16, 2)
