@@ -6,8 +6,8 @@
  *
  * The path, per training step: price the context chunks (Eq. 6), balance them
  * over P virtual ranks with cost-aware LPT (§4.2), compute every rank's local
- * partial attention (o_p, l_p) (Eq. 3, Alg. 1 line 7), merge the partials
- * exactly (Eq. 4, Alg. 1 line 8) and run the backward (Alg. 1 lines 12-21),
+ * partial attention (o_p, l_p) (Eq. 3, Alg. 1), merge the partials
+ * exactly (Eq. 4) and run the backward (Alg. 1's backward),
  * all on one GPU: the P ranks are a sweep over key/value chunks, and the
  * collectives of Alg. 1 become on-device passes.
  *
@@ -143,7 +143,7 @@ SKV_API size_t skv_workspace_bytes(const skv_problem* prob, int which);
 
 /*
  * Local partial attention of every virtual rank [Split-KV §4.1, Eq. 3;
- * Alg. 1 line 7]: for each rank p, each query row r and head h,
+ * the per-rank attention of Alg. 1]: for each rank p, each query row r and head h,
  *   z_x = scale * q_r . k_x  over the keys x in K_p with s_i <= x < a_i,
  *   lse_part[p][r][h] = log sum_x exp(z_x)          (natural log)
  *   o_part[p][r][h][:] = sum_x exp(z_x - lse) v_x
@@ -193,7 +193,7 @@ SKV_API skv_status skv_attn_fwd_static(const skv_problem* prob, const void* q, c
                                        void* stream);
 
 /*
- * Exact LSE merge of P disjoint partials [Split-KV §4.1, Eq. 4; Alg. 1 line 8]:
+ * Exact LSE merge of P disjoint partials [Split-KV §4.1, Eq. 4; the merge step of Alg. 1]:
  *   lse[r] = log sum_p exp(lse_part[p][r]),
  *   o[r][:] = sum_p exp(lse_part[p][r] - lse[r]) * o_part[p][r][:].
  * Partials with lse_part = -inf are skipped (their o_part row is not read);
@@ -235,10 +235,10 @@ SKV_API skv_status skv_lse_merge_bwd(const float* o_part, const float* lse_part,
 
 /*
  * Backward of the merged attention for L = sum(dO * o), lse receiving no
- * gradient [Split-KV Alg. 1 lines 12-21]: each virtual rank p produces dq^(p)
+ * gradient [Split-KV Alg. 1's backward]: each virtual rank p produces dq^(p)
  * and the dk_p, dv_p rows of its own chunks (the keys it holds); dq is the sum
- * of the dq^(p) over ranks (Alg. 1 line 17, made local).  The per-rank
- * MERGE_BWD of Alg. 1 line 15 is taken in its merged form: with
+ * of the dq^(p) over ranks (Alg. 1's dq reduce-scatter, made local).  The per-rank
+ * MERGE_BWD of Alg. 1 is taken in its merged form: with
  * D_r = dO_r . o_r and the global lse, the score gradient on rank p is
  * P_rx (dO_r . v_x - D_r) with P_rx = exp(z_rx - lse_r), which equals the
  * per-rank route exactly.
@@ -277,7 +277,7 @@ SKV_API skv_status skv_block_local_fwd(const skv_problem* prob, const void* q, c
 /*
  * Backward of the block-local term for L = sum(dO * o) of the whole mask,
  * with o and lse the MERGED results (context ranks + this term), the same
- * merged form as skv_attn_bwd [Alg. 1 line 15]: P = exp(z - lse), D = dO . o,
+ * merged form as skv_attn_bwd [Alg. 1's MERGE_BWD]: P = exp(z - lse), D = dO . o,
  * dS = P (dP - D).
  *   o                device [Q][H][d], dtype prob->dtype; lse device float[Q][H]
  *   dq               device float[Q][H][d], ACCUMULATED: call after

@@ -1,7 +1,7 @@
 // Tensor-core backward of the anchor attention (tcgen05 + TMEM + TMA), sm_103a.
 //
 // "Split-KV: Efficient Context Parallelism for Training Diffusion Drafters",
-// Alg. 1 lines 15-17 in merged form: with the global log-sum-exp l_r and
+// Alg. 1's backward in merged form: with the global log-sum-exp l_r and
 // D_r = dO_r . o_r, every rank's score gradient is dS = P (dP - D) with
 // P = exp(z - l).  Two kernels:
 //
@@ -20,7 +20,7 @@
 //  * attn_bwd_dq_tc_kernel -- query-stationary.  One thread block owns a
 //    128-row query tile and a head and walks, rank by rank, the key tiles of
 //    every rank's chunks that meet the tile's windows: dq = sum_p dq^(p)
-//    (Alg. 1 line 17) is accumulated in TMEM and written once.  Q and dO stay
+//    (Alg. 1's dq reduce-scatter) is accumulated in TMEM and written once.  Q and dO stay
 //    in TMEM as A operands; per key tile:
 //      S = Q K^T, dP = dO V^T (TS); eight warps form dS (bf16 -> TMEM over the
 //      dP they read); dQ += dS K (TS).  S of the next tile is issued as soon as

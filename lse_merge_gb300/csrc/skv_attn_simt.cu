@@ -10,7 +10,7 @@
 //
 // Forward: Eq. 3 of "Split-KV: Efficient Context Parallelism for Training
 // Diffusion Drafters" (§4.1) with an online (running max) softmax.
-// Backward: Alg. 1 lines 15-17 in merged form, P = exp(z - l_global),
+// Backward: Alg. 1's backward in merged form, P = exp(z - l_global),
 // dS = P (dP - D); dq^(p) is written per rank (summed by the dq-sum pass) and
 // dk, dv accumulate with fp32 atomics (several blocks see the same key; with
 // grouped queries, every query head of a key/value head's group too).

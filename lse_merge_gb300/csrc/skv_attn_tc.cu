@@ -1,7 +1,7 @@
 // Tensor-core anchor attention forward of libskv for GB300 (sm_103a): tcgen05
 // MMA with TMEM accumulators, TMA-fed bf16 operands, warp-specialised roles.
 //
-// Forward [Split-KV §4.1 Eq. 3; Alg. 1 line 7 of "Split-KV: Efficient Context
+// Forward [Split-KV §4.1 Eq. 3; the per-rank attention of Alg. 1 in "Split-KV: Efficient Context
 // Parallelism for Training Diffusion Drafters"]: one thread block computes the
 // partials (o_p, l_p) of two consecutive 128-row query tiles, one head and one
 // virtual rank p.  The key tiles it visits are the 128-key tiles of rank p's

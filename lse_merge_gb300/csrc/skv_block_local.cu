@@ -5,7 +5,7 @@
 // block tokens' own projections (k_blk, v_blk [Q][Hkv][d], rows as in q); they
 // form one more key set, disjoint from every context chunk, so the term is one
 // more partial (o, l) of Eq. 4 and its gradients use the merged o, l like the
-// context ranks do [Alg. 1 line 15 in merged form].
+// context ranks do [Alg. 1's MERGE_BWD in merged form].
 //
 // The work is B x B x d per (block, head) -- about 1e-4 of the context term at
 // the paper's sizes -- and reads/writes each row once: one 4-warp CTA per

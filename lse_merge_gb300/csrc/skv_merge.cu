@@ -1,7 +1,7 @@
 // Bandwidth-bound passes of libskv: the exact LSE merge of per-rank partials
-// [Split-KV §4.1, Eq. 4; Alg. 1 line 8], the backward pre-pass
-// D_r = dO_r . o_r (Alg. 1 line 15, merged form) and the dq sum over ranks
-// (Alg. 1 line 17 made local).  "Split-KV: Efficient Context Parallelism for
+// [Split-KV §4.1, Eq. 4; the merge step of Alg. 1], the backward pre-pass
+// D_r = dO_r . o_r (Alg. 1's MERGE_BWD, merged form) and the dq sum over ranks
+// (Alg. 1's dq reduce-scatter made local).  "Split-KV: Efficient Context Parallelism for
 // Training Diffusion Drafters".
 //
 // The merge is one HBM pass: G = d/4 lanes own one row (16-byte vectors, rows

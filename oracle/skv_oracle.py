@@ -280,7 +280,7 @@ def partition_forward(q, k, v, s, a, B: int, rank_of_chunk, m: int, P: int,
                       blocks: Optional[Sequence[int]] = None,
                       heads: Optional[Sequence[int]] = None):
     """Per-rank partials (o_p, l_p) for p < P over K_p  [Split-KV §4.1 Eq. 3,
-    Alg. 1 line 7].  Returns (o_part [P,Q,H,d], lse_part [P,Q,H])."""
+    the per-rank attention of Alg. 1].  Returns (o_part [P,Q,H,d], lse_part [P,Q,H])."""
     S = k.shape[0]
     outs, lses = [], []
     for p in range(P):
@@ -347,7 +347,7 @@ def attention_backward(q, k, v, s, a, B: int, dO, scale: Optional[float] = None,
       P_rx = exp(z_rx - l_r), dv_x = sum_r P_rx dO_r, dP_rx = dO_r . v_x,
       D_r = sum_x P_rx dP_rx, dS = P * (dP - D), dq_r = scale sum_x dS_rx k_x,
       dk_x = scale sum_r dS_rx q_r.
-    Split-KV computes the same gradients per rank (Alg. 1 lines 12-21) and sums
+    Split-KV computes the same gradients per rank (Alg. 1's backward) and sums
     dq over ranks; the partitioned route is ``partitioned_backward``.
     ``blocks`` restricts which query blocks contribute (dk/dv then hold only
     their contributions).  Returns (dq [Q,H,d], dk [S,Hkv,d], dv [S,Hkv,d])."""
@@ -549,7 +549,7 @@ def _given_backward(qb, kb, vb, gb, ob, lb, visible, scale):
 def context_backward_given(q, k, v, s, a, B: int, dO, o, lse, scale: Optional[float] = None,
                            blocks: Optional[Sequence[int]] = None, heads: Optional[Sequence[int]] = None):
     """The context part of the gradients of L = sum(dO * o) when o and lse are
-    the merged results of a larger key set (Alg. 1 line 15 in merged form):
+    the merged results of a larger key set (Alg. 1's MERGE_BWD in merged form):
     P_rx = exp(z_rx - l_r) over W_i, D_r = dO_r . o_r, dS = P (dP - D).
     With o, lse of the context alone this is ``attention_backward``.
     ``blocks``/``heads`` restrict which query rows contribute.  Returns (dq, dk, dv)."""
