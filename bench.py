@@ -53,15 +53,20 @@ TC_SOURCES = ("skv_attn_tc.cu", "skv_attn_bwd_tc.cu", "skv_ptx.cuh", "skv_tc.h",
 
 
 def csrc_digest():
-    """sha256 over the tensor-core kernels' sources: DRAM-traffic figures
-    captured with ncu are reported only while the kernels are the ones
-    captured."""
+    """sha256 over the tensor-core kernels' sources with comments and blank
+    lines left out: DRAM-traffic figures captured with ncu are reported only
+    while the kernels' code is the code that was captured."""
     import hashlib
+    import re
     h = hashlib.sha256()
     d = os.path.join(ROOT, "lse_merge_gb300", "csrc")
     for f in TC_SOURCES:
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+        h.update(f.encode() + b"\0" + code.encode())
     return h.hexdigest()
 
 

@@ -73,3 +73,23 @@ def test_merge_bytes_match_the_oracle_count():
         assert bench.merge_algorithmic_bytes(lse[:4], 16, out_b) == orc.merge_bytes(lse[:4].numpy(), 16, out_b)
         assert bench.merge_algorithmic_bytes(lse, 16, out_b) == orc.merge_bytes(lse.numpy(), 16, out_b)
     assert bench.merge_algorithmic_bytes(lse[:4], 16, 2) < bench.merge_algorithmic_bytes(lse, 16, 2)
+
+
+def test_traffic_digest_follows_code_not_comments(tmp_path, monkeypatch):
+    """The digest that gates the captured DRAM traffic ignores comment and
+    blank-line edits of the tensor-core kernels' sources and changes with any
+    code edit."""
+    import shutil
+    src = os.path.join(bench.ROOT, "lse_merge_gb300", "csrc")
+    dst = tmp_path / "lse_merge_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for f in bench.TC_SOURCES:
+        shutil.copy(os.path.join(src, f), dst / f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base = bench.csrc_digest()
+    f0 = dst / bench.TC_SOURCES[0]
+    text = f0.read_text()
+    f0.write_text("// a reworded comment\n\n/* and a block\n   comment */\n" + text)
+    assert bench.csrc_digest() == base
+    f0.write_text(text + "\nstatic const int digest_probe = 1;\n")   # one line of code more
+    assert bench.csrc_digest() != base
