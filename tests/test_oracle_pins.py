@@ -375,3 +375,23 @@ def test_useful_pairs_matches_profile():
 def test_merge_bytes_count():
     lp = np.array([[[0.0, -np.inf]], [[1.0, 2.0]]])   # P=2, rows=2, one empty partial
     assert orc.merge_bytes(lp, 4, 2) == 2 * 2 * 4 + 3 * 16 + 2 * (8 + 4)
+
+
+def test_mask_row_by_hand():
+    """Context window W_i = [s_i, a_i) as a boolean row [Split-KV §3.1, Fig. 1]:
+    the start is visible, the anchor itself is not."""
+    assert orc.mask_row(2, 5, 7).tolist() == [False, False, True, True, True, False, False]
+    assert not orc.mask_row(4, 4, 6).any()                 # empty window
+    assert orc.mask_row(0, 6, 6).all()                     # the whole context, a = S
+    assert orc.mask_row(3, 4, 5).tolist() == [False, False, False, True, False]
+
+
+def test_chunk_key_mask_by_hand():
+    """K_p: the keys of the chunks [j m, (j + 1) m) that rank p holds
+    [Split-KV §4.2]; the ranks' key sets partition the context."""
+    roc = [1, 0, 1, 2]                                     # chunks of m = 2 keys, S = 8
+    assert orc.chunk_key_mask(roc, 1, 2, 8).astype(int).tolist() == [1, 1, 0, 0, 1, 1, 0, 0]
+    assert orc.chunk_key_mask(roc, 0, 2, 8).astype(int).tolist() == [0, 0, 1, 1, 0, 0, 0, 0]
+    assert not orc.chunk_key_mask(roc, 3, 2, 8).any()     # a rank with no chunk
+    total = sum(orc.chunk_key_mask(roc, p, 2, 8).astype(int) for p in range(4))
+    assert total.tolist() == [1] * 8
