@@ -71,7 +71,8 @@ struct Chunk8<float> {
 // This thread's share of rows [iB, iB + B) of head h of a [Q][Hx][D] tensor:
 // chunk e = threadIdx.x + n * kThreads is row e / (D/8), columns 8 (e % (D/8)) + [0, 8).
 // load() issues every global load; store() writes them as fp32 shared rows of
-// stride D + 4.  NCH covers B <= 4 R rows.
+// stride D + 4.  The kernels take NCH = R D / 256, enough chunks for the B <= 4 R
+// rows of a CTA.
 template <typename T, int D, int NCH>
 struct Rows {
     static constexpr int PR = D / 8;   // chunks per row
@@ -127,9 +128,10 @@ __host__ __device__ inline int bwd_floats(int B, int d) { return 4 * B * (d + 4)
 
 // Dot products of this warp's rows r = w, w + 4, ... (R of them at most) with
 // key j, register-tiled: the lane keeps KC = 16 / NP of key j's columns per
-// pair in registers while the rows stream past as shared broadcasts.  R = 8 (B <= 32): key j is
-// lane j.  R = 4 (B <= 16): key j is lanes j and j + 16, each over half of the
-// columns.  NP operand pairs: (q, k), and (dO, v) too in the backward.
+// pair in registers while the rows stream past as shared broadcasts.  R = 8
+// (B <= 32): key j is lane j.  R = 4 (B <= 16): key j is lanes j and j + 16,
+// each over half of the columns.  NP operand pairs: (q, k), and (dO, v) too in
+// the backward.
 template <int D, int R, int NP>
 __device__ __forceinline__ void row_key_dots(const float* __restrict__ rows0, const float* __restrict__ keys0,
                                              const float* __restrict__ rows1, const float* __restrict__ keys1, int B,
@@ -253,11 +255,10 @@ block_local_fwd_kernel(const T* __restrict__ q, const T* __restrict__ kb, const 
 // key/value head); the query heads of the head's group (one head without
 // grouped queries) take turns.  Per query head: one batch of global loads (q,
 // dO, o rows and the rows' l; the dq values to add to are prefetched to L2),
-// then phase 1
-// (row_key_dots for q . k and dO . v) puts P and dS into shared memory; phase 2
-// (lanes over float4 columns) adds the dq rows of warp w's rows, and each thread
-// adds to the dk/dv columns it owns for warp w's keys j = w, w + 4, ..., kept in
-// registers over the whole group.
+// then phase 1 (row_key_dots for q . k and dO . v) puts P and dS into shared
+// memory; phase 2 (lanes over float4 columns) adds the dq rows of warp w's
+// rows, and each thread adds to the dk/dv columns it owns for warp w's keys
+// j = w, w + 4, ..., kept in registers over the whole group.
 template <typename T, int D, int R>
 __global__ void __launch_bounds__(kThreads, R == 4 ? 4 : 2)   // B <= 16: four CTAs an SM (128 registers)
 block_local_bwd_kernel(const T* __restrict__ q, const T* __restrict__ kb, const T* __restrict__ vb,
