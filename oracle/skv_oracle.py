@@ -341,7 +341,8 @@ def lse_merge_backward(o_part, lse_part, dO, dlse=None):
 
 def attention_backward(q, k, v, s, a, B: int, dO, scale: Optional[float] = None,
                        blocks: Optional[Sequence[int]] = None,
-                       heads: Optional[Sequence[int]] = None):
+                       heads: Optional[Sequence[int]] = None,
+                       kv_heads_only: bool = False):
     """Gradients of L = sum(dO * o) for the single-device masked attention
     (lse receives no gradient), textbook softmax backward:
       P_rx = exp(z_rx - l_r), dv_x = sum_r P_rx dO_r, dP_rx = dO_r . v_x,
@@ -350,7 +351,9 @@ def attention_backward(q, k, v, s, a, B: int, dO, scale: Optional[float] = None,
     Split-KV computes the same gradients per rank (Alg. 1's backward) and sums
     dq over ranks; the partitioned route is ``partitioned_backward``.
     ``blocks`` restricts which query blocks contribute (dk/dv then hold only
-    their contributions).  Returns (dq [Q,H,d], dk [S,Hkv,d], dv [S,Hkv,d])."""
+    their contributions).  Returns (dq [Q,H,d], dk [S,Hkv,d], dv [S,Hkv,d]);
+    with ``kv_heads_only`` dk and dv hold just the key/value heads of ``heads``,
+    in order of first use ([S, n, d]; the same sums, smaller arrays)."""
     s, a = _npi(s), _npi(a)
     N = len(s)
     Qn, H, d = q.shape
@@ -358,12 +361,17 @@ def attention_backward(q, k, v, s, a, B: int, dO, scale: Optional[float] = None,
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq = np.zeros((Qn, H, d))
-    dk = np.zeros((S, k.shape[1], d))
-    dv = np.zeros((S, k.shape[1], d))
     kv = _Heads(k, v, H)
-    for h in (range(H) if heads is None else heads):
+    hs = list(range(H) if heads is None else heads)
+    slot = {}
+    for h in hs:
+        slot.setdefault(kv.head(h), len(slot))
+    n_kv = len(slot) if kv_heads_only else k.shape[1]
+    dk = np.zeros((S, n_kv, d))
+    dv = np.zeros((S, n_kv, d))
+    for h in hs:
         kh, vh = kv.get(h)
-        c = kv.head(h)
+        c = slot[kv.head(h)] if kv_heads_only else kv.head(h)
         for i in (range(N) if blocks is None else blocks):
             rows = slice(i * B, (i + 1) * B)
             mrow = mask_row(int(s[i]), int(a[i]), S)
@@ -406,16 +414,23 @@ def backward_key_rows(q, k, v, s, a, B: int, dO, keys: Sequence[int],
             if not np.any((s[i] <= kidx) & (kidx < a[i])):
                 continue
             rows = slice(i * B, (i + 1) * B)
-            mrow = mask_row(int(s[i]), int(a[i]), S)
+            # the block's visible keys: the columns its mask row leaves open (a key
+            # outside them has exp(-inf) = 0 weight, so the row statistics are sums
+            # over these columns alone)
+            cols = np.flatnonzero(mask_row(int(s[i]), int(a[i]), S))
+            c0, c1 = int(cols[0]), int(cols[-1]) + 1      # one run of columns: the window [s_i, a_i)
+            assert c1 - c0 == len(cols)
             qb = _np64(q[rows, h, :])
             gb = _np64(dO[rows, h, :])
-            z = np.where(mrow[None, :], scale * (qb @ kh.T), NEG_INF)
-            e, ssum, _, empty = _softmax_stats(z)
-            Pm = np.where(empty[:, None], 0.0, e / np.where(empty, 1.0, ssum)[:, None])
-            dP = gb @ vh.T
+            z = scale * (qb @ kh[c0:c1].T)
+            e, ssum, _, _ = _softmax_stats(z)
+            Pm = e / ssum[:, None]
+            dP = gb @ vh[c0:c1].T
             D = (Pm * dP).sum(axis=1)
-            Pk = Pm[:, kidx]
-            dSk = Pk * (dP[:, kidx] - D[:, None])
+            pos = np.searchsorted(cols, kidx)          # the listed keys' columns among the visible ones
+            seen = (pos < len(cols)) & (cols[np.minimum(pos, len(cols) - 1)] == kidx)
+            Pk = np.where(seen[None, :], Pm[:, np.minimum(pos, len(cols) - 1)], 0.0)
+            dSk = Pk * (dP[:, np.minimum(pos, len(cols) - 1)] - D[:, None])
             dv[:, hi, :] += Pk.T @ gb
             dk[:, hi, :] += scale * (dSk.T @ qb)
     return dk, dv

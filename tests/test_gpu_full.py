@@ -13,7 +13,9 @@ from workloads import LONG_1M, PACKED, PACKED_KV8, make_inputs, qs_sweep
 
 pytestmark = pytest.mark.gpu
 
-FULL = [PACKED, LONG_1M, qs_sweep(4, "contiguous"), qs_sweep(32, "lpt"), PACKED_KV8]
+# every Q:S ratio of the sweep once, the two chunk orders alternating
+FULL = [PACKED, LONG_1M, qs_sweep(4, "contiguous"), qs_sweep(8, "lpt"), qs_sweep(16, "contiguous"),
+        qs_sweep(32, "lpt"), PACKED_KV8]
 
 
 def sample_blocks(N, seed):
@@ -126,6 +128,22 @@ def test_full_dkdv_sampled_keys(full_run):
     kt = torch.as_tensor(keys, device="cuda")
     assert maxabs(dk[kt][:, heads].cpu().numpy(), r_dk) <= TOL_BF16
     assert maxabs(dv[kt][:, heads].cpu().numpy(), r_dv) <= TOL_BF16
+
+
+def test_full_dkdv_prompt_keys(full_run):
+    """Keys of the first sample's prompt quarter: every block of the sample sees
+    them, so their key tiles walk every query tile of the sample in the
+    key-stationary pass (the path that dominates the backward).  Key/value head
+    0 only, on the workloads whose samples the oracle walks in seconds."""
+    w, inp, prob, _, _, _, _, _, dq, dk, dv = full_run
+    if w.name not in ("packed_4x128k", "qs_1to32_lpt"):
+        pytest.skip("the oracle's walk over every block of a sample is too long here")
+    L = w.sample_len
+    keys = [0, 131, L // 8 + 77, L // 4 - 1]
+    r_dk, r_dv = orc.backward_key_rows(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, inp.dO, keys, [0])
+    kt = torch.as_tensor(keys, device="cuda")
+    assert maxabs(dk[kt][:, [0]].cpu().numpy(), r_dk) <= TOL_BF16
+    assert maxabs(dv[kt][:, [0]].cpu().numpy(), r_dv) <= TOL_BF16
 
 
 def test_full_gradient_properties(full_run):

@@ -15,6 +15,7 @@ import torch
 import torch.nn.functional as F
 
 import oracle as orc
+from workloads import make_inputs, random_small
 from test_oracle_pins import rand_problem
 
 
@@ -126,3 +127,17 @@ def test_gqa_block_local_term_vs_sdpa():
         tv += rv[:S]
     np.testing.assert_allclose(ck, tk, atol=1e-12)
     np.testing.assert_allclose(cv, tv, atol=1e-12)
+
+
+def test_backward_kv_heads_only_selects_the_same_sums():
+    # the compact dk/dv of kv_heads_only are the full arrays' columns of the
+    # key/value heads in use, in order of first use (here heads 5 then 0 of an
+    # 8-over-2 layout: key/value heads 1, then 0)
+    w = random_small(71, 1, 384, 5, 4, 8, 16, 128, 3, "fp32").with_(Hkv=2)
+    inp = make_inputs(w)
+    full = orc.attention_backward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, inp.dO, heads=[5, 0])
+    part = orc.attention_backward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, inp.dO, heads=[5, 0], kv_heads_only=True)
+    assert np.array_equal(full[0], part[0])
+    for f, p_ in zip(full[1:], part[1:]):
+        assert p_.shape == (w.S, 2, w.d)
+        assert np.array_equal(f[:, 1], p_[:, 0]) and np.array_equal(f[:, 0], p_[:, 1])

@@ -82,6 +82,40 @@ def test_lpt_hand_example():
     assert order.tolist() == [0, 3, 5, 1, 2, 4]
 
 
+def test_contiguous_hand_example():
+    # "No balance" keeps the contiguous assignment: rank p holds the context shard
+    # of S/P consecutive rows, i.e. chunks [pJ, (p+1)J) [Split-KV §5.1 Baselines;
+    # §5.2: the local shard stays S/P rows per rank].  Worked by hand for 6 chunks,
+    # P = 3, J = 2 with costs [7, 1, 4, 4, 0, 9]: loads 7+1, 4+4, 0+9.
+    roc, order, load = orc.contiguous_assign(6, 3, 2, [7, 1, 4, 4, 0, 9])
+    assert roc.tolist() == [0, 0, 1, 1, 2, 2]
+    assert order.tolist() == [0, 1, 2, 3, 4, 5]
+    assert load.tolist() == [8, 8, 9]
+    # without costs the loads are zeros (the map alone)
+    roc2, order2, load2 = orc.contiguous_assign(6, 2, 3)
+    assert roc2.tolist() == [0, 0, 0, 1, 1, 1] and order2.tolist() == list(range(6))
+    assert load2.tolist() == [0, 0]
+    with pytest.raises(ValueError):
+        orc.contiguous_assign(7, 3, 2)
+
+
+def test_fig5_contiguous_loads_are_the_shards():
+    # Fig. 5's 12 two-token chunks (printed costs 16,16,16 | 12,12,6 | 0,0,16 |
+    # 12,6,0) over P = 4 ranks with J = 3: summed by hand, 48, 30, 16, 18.  The
+    # same loads come from Eq. 2's profile summed over each rank's contiguous
+    # shard of S/P = 6 rows, a route that never forms chunks.
+    g, s, a = fig5()
+    S = sum(g["sample_lens"])
+    roc, order, load = orc.contiguous_assign(12, g["P"], g["J"], g["chunk_costs"])
+    assert roc.tolist() == [0, 0, 0, 1, 1, 1, 2, 2, 2, 3, 3, 3]
+    assert load.tolist() == [48, 30, 16, 18]
+    prof = orc.anchor_profile(s, a, g["B"], S)
+    shard = S // g["P"]
+    assert [orc.rank_load(prof, range(p * shard, (p + 1) * shard)) for p in range(g["P"])] == [48, 30, 16, 18]
+    # rho with the page's D = (N/P) B^2 = 8: max W = 56 over mean W = 36
+    assert abs(orc.imbalance(load, len(s), g["P"], g["B"]) - 56 / 36) < 1e-12
+
+
 def test_lpt_j1_closed_form():
     # With J = 1 every rank takes one chunk: the p-th costliest goes to rank p.
     rng = np.random.default_rng(3)
