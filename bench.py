@@ -33,7 +33,7 @@ if ROOT not in sys.path:
 
 METRIC = "anchor-attn fwd+bwd useful TFLOP/s and % BF16 tensor peak; merge HBM GB/s"
 UNIT = "TFLOP/s"
-DEFAULT_WORKLOAD = "packed_4x128k"
+DEFAULT_WORKLOAD = "qs_1to32_lpt"   # the largest single-GPU configuration (S = 2M keys, Q = 64k)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -177,28 +177,41 @@ def useful_pairs_per_head(s, a, B):
 def oracle_sample(w, inp, budget_s: float, block_offset: int = 0):
     """Times the CPU oracle (as it stands) on a bounded sample of the workload:
     forward (+ backward when the workload has one) of whole query blocks of one
-    head, until ~budget_s seconds of work.  Returns (TFLOP/s useful, desc)."""
+    head, until ~budget_s seconds of work.  A block's window lies inside its own
+    sample, so each block is given its sample's keys and values (the oracle's
+    mask row covers those L keys; every key outside them is masked for the
+    block) and the backward keeps dk, dv of the one key/value head in use.
+    Returns (useful TFLOP/s, description, seconds, extrapolated step seconds)."""
     import oracle as orc
-    N = w.N
+    N, L = w.N, w.sample_len
     stride = max(1, N // 64)
     order = [(block_offset + t * stride) % N for t in range(N)]
     head = 0
+    s_all, a_all = inp.s.long(), inp.a.long()
     t0 = time.perf_counter()
     pairs = 0
     done = []
     for i in order:
-        orc.attention_forward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, blocks=[i], heads=[head])
+        u0 = int(s_all[i]) // L * L                  # the block's sample: keys [u0, u0 + L)
+        k_u, v_u = inp.k[u0:u0 + L], inp.v[u0:u0 + L]
+        s_u, a_u = s_all - u0, a_all - u0
+        orc.attention_forward(inp.q, k_u, v_u, s_u, a_u, w.B, blocks=[i], heads=[head])
         if w.backward:
-            orc.attention_backward(inp.q, inp.k, inp.v, inp.s, inp.a, w.B, inp.dO, blocks=[i], heads=[head])
+            orc.attention_backward(inp.q, k_u, v_u, s_u, a_u, w.B, inp.dO, blocks=[i], heads=[head],
+                                   kv_heads_only=True)
         pairs += w.B * max(0, int(inp.a[i]) - int(inp.s[i]))
         done.append(i)
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
     flops = pairs * w.d * (12 if w.backward else 4)
-    desc = (f"{len(done)} query blocks (B={w.B} rows each) x head {head} of {w.name}, "
-            f"{'fwd+bwd' if w.backward else 'fwd'}, {pairs} useful pairs, {dt:.1f} s")
-    return flops / dt / 1e12, desc, dt
+    desc = (f"{len(done)} query blocks (B={w.B} rows each) x head {head} of {w.name}, each over its "
+            f"sample's {L} keys, {'fwd+bwd' if w.backward else 'fwd'}, {pairs} useful pairs, {dt:.1f} s")
+    # the oracle's cost per (block, head) does not depend on the window (it forms
+    # the explicit mask row and the scores over all L keys of the sample), so the
+    # whole step scales with the number of (block, head) pairs
+    extrap_s = dt * (w.N * w.H) / max(1, len(done))
+    return flops / dt / 1e12, desc, dt, extrap_s
 
 
 def blas_threads():
@@ -281,7 +294,7 @@ def run_reference(args):
     inp = make_inputs(w, device="cuda" if torch.cuda.is_available() else "cpu")
     per_step = []
     for t in range(args.warmup + args.steps):
-        tf, desc, dt = oracle_sample(w, inp, args.ref_step_s, block_offset=7 * t)
+        tf, desc, dt, _ = oracle_sample(w, inp, args.ref_step_s, block_offset=7 * t)
         if t >= args.warmup:
             per_step.append((tf, dt, desc))
     value = statistics.mean(x[0] for x in per_step)
@@ -468,6 +481,7 @@ def run_ours(args):
         mb_bytes = P * Q * H * 4 + fin_c * d * 4 + Q * H * d * eb_do + P * Q * H * 4 + P * Q * H * d * 4
         mbwd = {"ms": mb_ms, "bytes": mb_bytes, "gbs": mb_bytes / (mb_ms * 1e-3) / 1e9}
         del do_part, dlse_part
+        torch.cuda.empty_cache()
 
     pairs = useful_pairs_per_head(inp.s, inp.a, w.B) * H
     fwd_flops = 4.0 * d * pairs
@@ -515,6 +529,17 @@ def run_ours(args):
         if per_pair and tr.get("csrc_sha256") == csrc_digest():
             traffic = per_pair * pairs
 
+    # the CPU baseline before the end-to-end pass: the pinned host buffers of the
+    # largest workloads and the oracle's arrays do not fit in host memory together
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, desc, _, extrap_s = oracle_sample(w, inp, args.cpu_budget_s)
+        cpu = {"value": tf, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc,
+               "extrapolated_full_step_s": extrap_s,
+               "extrapolation": f"sample time x (N x H = {w.N} x {w.H}) / blocks sampled: the oracle's "
+                                "cost per (block, head) is the same for every block (explicit mask row over "
+                                "its sample's L keys); extrapolated, not measured"}
+
     # end to end through the public API with host buffers (pinned), copies inside
     e2e = None
     if not args.no_e2e and w.backward:
@@ -546,60 +571,59 @@ def run_ours(args):
         torch.cuda.synchronize()
         serial_ms = t_s.elapsed_time(t_e) / ke
 
-        # pipelined: two device sets; step t+1's inputs go up (one copy stream) and
-        # step t's results come down (another) while step t computes.  Every step
-        # still copies all of its inputs in and all of its results out.
-        def dev_set():
-            s2, a2 = torch.empty_like(s), torch.empty_like(a)
-            st = {"s": s2, "a": a2, "q": torch.empty_like(q), "k": torch.empty_like(k), "v": torch.empty_like(v),
-                  "dO": torch.empty_like(dO), "o_part": torch.empty_like(o_part[:P]),
-                  "lse_part": torch.empty_like(lse_part[:P]), "o": torch.empty_like(o), "lse": torch.empty_like(lse),
-                  "dq": torch.empty_like(dq), "dk": torch.empty_like(dk), "dv": torch.empty_like(dv),
-                  "costs": torch.empty_like(costs), "ws_f": torch.empty_like(ws_f), "ws_b": torch.empty_like(ws_b)}
-            st["prob"] = skv.Problem(s2, a2, w.B, H, d, w.S, w.m, P, tdt, n_kv_heads=w.Hkv)
-            return st
-
-        sets = [dev_set(), dev_set()]
+        # pipelined: the inputs have two device sets (the resident one and a second),
+        # the results one (the resident buffers).  Step t+1's inputs go up on one copy
+        # stream while step t computes; step t's results come down on another while
+        # step t+1 plans and runs its forward; step t+1's merge and backward wait
+        # until the results they overwrite are down.  Every step still copies all of
+        # its inputs in and all of its results out.
         names_in = ("s", "a", "q", "k", "v", "dO")
-        names_out = ("o", "lse", "dq", "dk", "dv")
+        in_sets = [dict(zip(names_in, (s, a, q, k, v, dO)))]
+        in_sets.append({nm: torch.empty_like(x) for nm, x in in_sets[0].items()})
+        probs = [skv.Problem(st["s"], st["a"], w.B, H, d, w.S, w.m, P, tdt, n_kv_heads=w.Hkv) for st in in_sets]
         h_src = [hsrc for hsrc, _ in h_in]
-        h_dst = [h_o, h_lse, h_dq, h_dk, h_dv]
+        h_small = [(o, h_o), (lse, h_lse)]
+        h_big = [(dq, h_dq), (dk, h_dk), (dv, h_dv)]
         up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         comp = torch.cuda.current_stream(dev)
         ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_done = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
-
-        def run_set(st):
-            pr = st["prob"]
-            skv.chunk_costs(pr, st["costs"])
-            if w.order == "lpt":
-                roc_s, _, _ = skv.lpt_order(st["costs"], P, w.J)
-            else:
-                roc_s, _, _ = skv.contiguous_order(w.n_chunks, P, w.J, st["costs"])
-            skv.attn_fwd(pr, st["q"], st["k"], st["v"], roc_s, st["o_part"], st["lse_part"], st["ws_f"])
-            skv.lse_merge(st["o_part"], st["lse_part"], o=st["o"], lse=st["lse"])
-            skv.attn_bwd(pr, st["q"], st["k"], st["v"], st["o"], st["lse"], st["dO"], roc_s, st["dq"], st["dk"],
-                         st["dv"], st["ws_b"])
+        ev_used = [torch.cuda.Event() for _ in range(2)]
+        ev_done, ev_small, ev_big = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+        started = [False]
 
         def pipelined(n_steps):
             for t in range(n_steps):
                 b = t % 2
-                st = sets[b]
+                st, pr = in_sets[b], probs[b]
                 with torch.cuda.stream(up):
-                    up.wait_event(ev_done[b])            # step t-2 has finished with these inputs
+                    up.wait_event(ev_used[b])            # step t-2 has finished with these inputs
                     for hs, nm in zip(h_src, names_in):
                         st[nm].copy_(hs, non_blocking=True)
                     ev_in[b].record(up)
                 comp.wait_event(ev_in[b])
-                comp.wait_event(ev_out[b])               # step t-2's results of this set are down
-                run_set(st)
-                ev_done[b].record(comp)
+                skv.chunk_costs(pr, costs)
+                if w.order == "lpt":
+                    roc_s, _, _ = skv.lpt_order(costs, P, w.J)
+                else:
+                    roc_s, _, _ = skv.contiguous_order(w.n_chunks, P, w.J, costs)
+                skv.attn_fwd(pr, st["q"], st["k"], st["v"], roc_s, o_part[:P], lse_part[:P], ws_f)
+                if started[0]:
+                    comp.wait_event(ev_small)            # step t-1's o and lse are down
+                skv.lse_merge(o_part[:P], lse_part[:P], o=o, lse=lse)
+                if started[0]:
+                    comp.wait_event(ev_big)              # step t-1's dq, dk and dv are down
+                skv.attn_bwd(pr, st["q"], st["k"], st["v"], o, lse, st["dO"], roc_s, dq, dk, dv, ws_b)
+                ev_used[b].record(comp)
+                ev_done.record(comp)
+                started[0] = True
                 with torch.cuda.stream(down):
-                    down.wait_event(ev_done[b])
-                    for nm, hd in zip(names_out, h_dst):
-                        hd.copy_(st[nm], non_blocking=True)
-                    ev_out[b].record(down)
+                    down.wait_event(ev_done)
+                    for dsrc, hdst in h_small:
+                        hdst.copy_(dsrc, non_blocking=True)
+                    ev_small.record(down)
+                    for dsrc, hdst in h_big:
+                        hdst.copy_(dsrc, non_blocking=True)
+                    ev_big.record(down)
             comp.wait_stream(up)
             comp.wait_stream(down)
 
@@ -613,20 +637,16 @@ def run_ours(args):
         if skv.stream_status() != 0:
             raise RuntimeError("device status set during the end-to-end pass")
         e_ms = t_s.elapsed_time(t_e) / kp
-        del sets
+        del in_sets, probs, h_in, h_small, h_big, h_src, h_out, h_o, h_lse, h_dq, h_dk, h_dv
         e_ms, serial_ms = slowest([e_ms, serial_ms], world, dev)
         e2e = {"value": job_tflops(step_flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "mode": f"pipelined over {kp} steps: step t+1's inputs up and step t's results down "
-                       "on two copy streams while step t computes (two device buffer sets); the first "
-                       "step's upload and the last step's download, which nothing overlaps, are inside "
-                       "the timed region",
+               "mode": f"pipelined over {kp} steps: step t+1's inputs go up on one copy stream while "
+                       "step t computes (two device input sets), step t's results come down on another "
+                       "while step t+1 plans and runs its forward (one result set: step t+1's merge and "
+                       "backward wait for that download); the first upload and the last download are "
+                       "inside the timed region",
                "serial": {"ms_per_step": serial_ms, "value": job_tflops(step_flops, world, serial_ms)}}
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, desc, _ = oracle_sample(w, inp, args.cpu_budget_s)
-        cpu = {"value": tf, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc}
 
     if rank == 0:
         line = {
@@ -643,6 +663,11 @@ def run_ours(args):
                               "nominal_2250": value / world / 2250.0},
             "phases_ms": ph,
             "useful_tflop_per_step": step_flops / 1e12,
+            "fa_convention": ({"label": "secondary: FlashAttention convention, backward credited 10 d FLOP per "
+                                        "pair (its recomputed Q K^T counted), forward 4 d",
+                               "tflop_per_step": (fwd_flops + 10.0 * d * pairs) / 1e12,
+                               "value": job_tflops(fwd_flops + 10.0 * d * pairs, world, ms)}
+                              if w.backward else None),
             "merge": {"gbs": merge_gbs, "bytes": merge_bytes, "frac_of_hbm": merge_gbs / hbm,
                       "peak_gbs": hbm, "peak_kind": pk_kind},
             "roofline": {"kernel": dom, "bound": "tensor", "achieved": dom_tf,

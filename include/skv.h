@@ -174,7 +174,8 @@ SKV_API skv_status skv_attn_fwd(const skv_problem* prob, const void* q, const vo
  *
  * Same arguments, semantics and outputs as skv_attn_fwd.  The scratch the
  * forward needs (the per-rank chunk lists, 4 bytes per chunk and per rank, and
- * the key bounds of each 128-row query tile, 16 bytes each) lives in a fixed
+ * the key bounds of each 128-row query tile, 16 bytes each, counted only for
+ * bf16 problems, whose tensor-core forward uses them) lives in a fixed
  * 128 KiB array in device memory that every GPU loading the library holds
  * until the process exits; the call itself allocates nothing.  Problems whose
  * forward workspace (skv_workspace_bytes(prob, 0)) exceeds 131072 bytes are
@@ -186,7 +187,9 @@ SKV_API skv_status skv_attn_fwd(const skv_problem* prob, const void* q, const vo
  * capture.  All calls share the one array, and each call rewrites the lists
  * before reading them (nothing in it has to start at zero), so calls that
  * overlap on the GPU (on different streams, or from different host threads
- * without ordering) race and must be serialised by the caller.
+ * without ordering) race and must be serialised by the caller.  The address is
+ * kept for the life of the process, like the status word's: do not use the
+ * library across cudaDeviceReset of a device it has run on.
  */
 SKV_API skv_status skv_attn_fwd_static(const skv_problem* prob, const void* q, const void* k, const void* v,
                                        const int32_t* rank_of_chunk, float* o_part, float* lse_part,

@@ -452,7 +452,8 @@ bool fwd_supported(const skv_problem& pb) {
            pb.P <= 65535 && pb.n_heads <= 65535 && pb.S <= INT32_MAX &&
            int64_t(pb.n_blocks) * pb.B <= INT32_MAX;
 }
-size_t fwd_scratch_bytes(const skv_problem& pb) {   // per query tile key bounds (int4)
+size_t fwd_scratch_bytes(const skv_problem& pb) {   // per query tile key bounds (int4); none off this path
+    if (!fwd_supported(pb)) return 0;
     const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
     return size_t((Qn + BM - 1) / BM) * sizeof(int4);
 }

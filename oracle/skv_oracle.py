@@ -339,6 +339,31 @@ def lse_merge_backward(o_part, lse_part, dO, dlse=None):
     return do_part, dlse_part
 
 
+def merge_oproj(o_part, lse_part, w_o):
+    """The output projection fused with the merge  [Split-KV §4.1, Eq. 5; the
+    MERGE_AR, OProj and RS_sum steps of Alg. 1's forward]: every rank scales its
+    partial by its merge weight, o_bar_p = exp(l_p - l) o_p (zero where
+    l_p = -inf), projects it, OProj(x) = x W_o^T over the concatenated heads,
+    and the projected outputs are summed over the ranks:
+        Y = sum_p OProj(o_bar_p).
+    Taken in that order here (one projection per partial).  o_part
+    [P, Q, H, d], lse_part [P, Q, H], w_o [d_model, H*d]; returns
+    (Y [Q, d_model], l [Q, H])."""
+    o_part = np.asarray(_np64(o_part), np.float64)
+    lse_part = np.asarray(_np64(lse_part), np.float64)
+    w = np.asarray(_np64(w_o), np.float64)
+    P, Qn, H, d = o_part.shape
+    _, lse = lse_merge(o_part, lse_part)
+    fin = np.isfinite(lse_part)
+    lse_safe = np.where(np.isfinite(lse), lse, 0.0)
+    y = np.zeros((Qn, w.shape[0]))
+    for p in range(P):
+        wp = np.where(fin[p], np.exp(np.where(fin[p], lse_part[p], 0.0) - lse_safe), 0.0)   # [Q, H]
+        o_bar = np.where(fin[p][..., None], wp[..., None] * o_part[p], 0.0)                # [Q, H, d]
+        y += o_bar.reshape(Qn, H * d) @ w.T
+    return y, lse
+
+
 def attention_backward(q, k, v, s, a, B: int, dO, scale: Optional[float] = None,
                        blocks: Optional[Sequence[int]] = None,
                        heads: Optional[Sequence[int]] = None,
