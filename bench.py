@@ -330,7 +330,7 @@ def run_ours(args):
         dist.barrier()
     import lse_merge_gb300 as skv
     from lse_merge_gb300 import _lib
-    from workloads import WORKLOADS, block_kv, make_inputs
+    from workloads import WORKLOADS, block_kv, make_inputs, oproj_weight
 
     lib = _lib.load()
     w = WORKLOADS[args.workload]
@@ -388,7 +388,7 @@ def run_ours(args):
 
     kt_names = ["attn_fwd_tc_kernel", "lse_merge_kernel", "attn_bwd_dkdv_tc_kernel", "attn_bwd_dq_tc_kernel",
                 "block_local_fwd_kernel", "block_local_bwd_kernel"]
-    kt_buf = (ctypes.c_float * 6)()
+    kt_buf = (ctypes.c_float * 7)()
     for _ in range(args.warmup):
         path()
     torch.cuda.synchronize()
@@ -459,6 +459,34 @@ def run_ours(args):
 
     # the per-partial merge backward (MERGE_BWD of Alg. 1, the route a multi-GPU
     # build takes) on this step's context partials: timed on its own, not in the step
+    # Eq. 5: the merge with the output projection (Table 2's d_model = 2048) on this
+    # step's context partials, its own pass
+    oproj = None
+    if tdt == torch.bfloat16:
+        d_model = 2048
+        w_o = oproj_weight(w.seed + 11, d_model, H * d, device=str(dev))
+        y_o = torch.empty(Q, d_model, dtype=torch.float32, device=dev)
+        skv.lse_merge_oproj(o_part[:P], lse_part[:P], w_o, o=o, lse=lse, y=y_o)
+        torch.cuda.synchronize()
+        lib.skv_set_kernel_timing(1)
+        skv.lse_merge_oproj(o_part[:P], lse_part[:P], w_o, o=o, lse=lse, y=y_o)
+        g_ms = kt_buf[6] if lib.skv_kernel_times(kt_buf, 7) == 0 and kt_buf[6] >= 0 else None
+        lib.skv_set_kernel_timing(0)
+        o_s, o_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        o_s.record()
+        for _ in range(n_kt):
+            skv.lse_merge_oproj(o_part[:P], lse_part[:P], w_o, o=o, lse=lse, y=y_o)
+        o_e.record()
+        torch.cuda.synchronize()
+        if skv.stream_status() != 0:
+            raise RuntimeError("device status set by the merge with the output projection")
+        op_ms = o_s.elapsed_time(o_e) / n_kt
+        gflop = 2.0 * Q * d_model * H * d
+        oproj = {"d_model": d_model, "ms": op_ms, "gemm_ms": g_ms,
+                 "gemm_tflops": gflop / (g_ms * 1e-3) / 1e12 if g_ms else None,
+                 "route": "Eq. 4 merge into o (bf16), then y = o W_o^T on the tensor cores (one C-ABI call)"}
+        del w_o, y_o
+
     mbwd = None
     if w.backward:
         do_part = torch.empty(P, Q, H, d, dtype=torch.float32, device=dev)
@@ -678,6 +706,7 @@ def run_ours(args):
                             "whole_mask_ms_per_step": whole_ms,
                             "fwd": kernels.get("block_local_fwd_kernel"),
                             "bwd": kernels.get("block_local_bwd_kernel")},
+            "merge_oproj": oproj,
             "merge_bwd": (dict(mbwd, frac_of_hbm=mbwd["gbs"] / hbm, peak_kind=pk_kind,
                                route="per-partial MERGE_BWD on this step's partials (own pass)")
                           if mbwd else None),

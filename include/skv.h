@@ -211,6 +211,32 @@ SKV_API skv_status skv_lse_merge(const float* o_part, const float* lse_part, int
                          int32_t head_dim, void* o, skv_dtype o_dtype, float* lse, void* stream);
 
 /*
+ * The merge fused with the output projection [Split-KV §4.1, Eq. 5; the
+ * MERGE_AR, OProj and RS_sum steps of Alg. 1's forward]: with the merge
+ * weights w_p = exp(lse_part[p] - lse) of Eq. 4 and OProj(x) = x W_o^T over the
+ * concatenated heads,
+ *   y = sum_p OProj(w_p o_part[p]) = OProj(o),   o = sum_p w_p o_part[p].
+ * The sum is linear, so it is taken before the projection: o and lse are
+ * written exactly as skv_lse_merge writes them (o in bf16), then a tensor-core
+ * GEMM computes y = o W_o^T from the bf16 o (fp32 accumulation).
+ *   o_part   device float[P][Q][n_heads][head_dim]
+ *   lse_part device float[P][Q][n_heads]
+ *   w_o      device bf16 [d_model][n_heads*head_dim], row-major (the projection's
+ *            weight; caller-owned)
+ *   o        device bf16 [Q][n_heads][head_dim], written (the merged output,
+ *            which the backward reads); 16-byte aligned
+ *   lse      device float[Q][n_heads], written (may be NULL)
+ *   y        device float[Q][d_model], written
+ * head_dim in {64, 128, 256}; d_model a multiple of 16; w_o, o, y and o_part
+ * 16-byte aligned.  Rows whose partials are all empty get o = 0 and add
+ * nothing to y.  Errors: SKV_ERR_INVALID_ARG / SKV_ERR_UNSUPPORTED before any
+ * launch; SKV_ERR_TIMEOUT through skv_stream_status.
+ */
+SKV_API skv_status skv_lse_merge_oproj(const float* o_part, const float* lse_part, int32_t P, int64_t Q,
+                                       int32_t n_heads, int32_t head_dim, const void* w_o, int32_t d_model,
+                                       void* o, float* lse, float* y, void* stream);
+
+/*
  * Backward of the exact LSE merge, per partial [Split-KV §4.1, Eq. 4; the
  * MERGE_BWD step of Alg. 1's backward]: for upstream gradients dO (of o) and
  * dlse (of lse), with the merged lse and o of skv_lse_merge,
@@ -326,7 +352,7 @@ SKV_API uint64_t skv_launch_count(void);
  * CUDA event pair on the launching stream around each of its main kernels:
  * slot 0 the forward attention kernel, 1 the LSE merge, 2 the backward dK/dV
  * kernel, 3 the backward dQ kernel (tensor-core path), 4 and 5 the
- * block-local forward and backward.  skv_kernel_times
+ * block-local forward and backward, 6 the output-projection GEMM.  skv_kernel_times
  * waits for the last recorded pair of each of the first n slots and writes
  * its duration in milliseconds (-1 where nothing was recorded since the
  * previous read).  Off by default; the events are created on first use.

@@ -20,7 +20,7 @@ from . import _lib
 from ._lib import SKV_BF16, SKV_FP32, SkvProblem
 
 __all__ = ["SkvError", "Problem", "chunk_costs", "lpt_order", "contiguous_order", "zigzag_loads",
-           "workspace_bytes", "attn_fwd", "attn_fwd_static", "lse_merge", "lse_merge_bwd", "attn_bwd", "stream_status", "set_wait_limit",
+           "workspace_bytes", "attn_fwd", "attn_fwd_static", "lse_merge", "lse_merge_bwd", "lse_merge_oproj", "attn_bwd", "stream_status", "set_wait_limit",
            "forward", "plan", "block_local_fwd", "block_local_bwd"]
 
 
@@ -179,6 +179,25 @@ def lse_merge(o_part: torch.Tensor, lse_part: torch.Tensor, out_dtype: torch.dty
     _check(_lib.load().skv_lse_merge(_ptr(o_part), _ptr(lse_part), P, rows, d, _ptr(o), _dtype_code(o.dtype),
                                      _ptr(lse), _stream()), "skv_lse_merge")
     return o, lse
+
+
+def lse_merge_oproj(o_part: torch.Tensor, lse_part: torch.Tensor, w_o: torch.Tensor,
+                    o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                    y: Optional[torch.Tensor] = None):
+    """Eq. 5: the merge of the partials [P, Q, H, d] and the output projection
+    y = o W_o^T (w_o bf16 [d_model, H*d]).  Returns (y fp32 [Q, d_model],
+    o bf16 [Q, H, d], lse fp32 [Q, H])."""
+    P, Q, H, d = o_part.shape
+    d_model = w_o.shape[0]
+    dev = o_part.device
+    o = torch.empty(Q, H, d, dtype=torch.bfloat16, device=dev) if o is None else o
+    lse = torch.empty(Q, H, dtype=torch.float32, device=dev) if lse is None else lse
+    y = torch.empty(Q, d_model, dtype=torch.float32, device=dev) if y is None else y
+    if w_o.dtype != torch.bfloat16 or o.dtype != torch.bfloat16 or y.dtype != torch.float32:
+        raise ValueError("w_o and o are bf16, y is fp32")
+    _check(_lib.load().skv_lse_merge_oproj(_ptr(o_part), _ptr(lse_part), P, Q, H, d, _ptr(w_o), d_model, _ptr(o),
+                                           _ptr(lse), _ptr(y), _stream()), "skv_lse_merge_oproj")
+    return y, o, lse
 
 
 def lse_merge_bwd(o_part: torch.Tensor, lse_part: torch.Tensor, dO: torch.Tensor, dlse: Optional[torch.Tensor] = None,

@@ -24,6 +24,8 @@ SIGNATURES = {
     "skv_lse_merge": (c_int, [c_void_p, c_void_p, c_int32, c_int64, c_int32, c_void_p, c_int, c_void_p, c_void_p]),
     "skv_lse_merge_bwd": (c_int, [c_void_p, c_void_p, c_int32, c_int64, c_int32, c_void_p, c_int, c_void_p, c_void_p,
                                   c_void_p, c_void_p]),
+    "skv_lse_merge_oproj": (c_int, [c_void_p, c_void_p, c_int32, c_int64, c_int32, c_int32, c_void_p, c_int32,
+                                    c_void_p, c_void_p, c_void_p, c_void_p]),
     "skv_attn_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "skv_stream_status": (c_int, [c_void_p]),

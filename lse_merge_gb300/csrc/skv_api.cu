@@ -254,6 +254,29 @@ skv_status skv_lse_merge(const float* o_part, const float* lse_part, int32_t P, 
     return skv_internal::launch_merge(o_part, lse_part, P, rows, head_dim, o, o_dtype, lse, c);
 }
 
+skv_status skv_lse_merge_oproj(const float* o_part, const float* lse_part, int32_t P, int64_t Q, int32_t n_heads,
+                              int32_t head_dim, const void* w_o, int32_t d_model, void* o, float* lse, float* y,
+                              void* stream) {
+    if (P < 1 || Q < 0 || n_heads < 1 || d_model < 16 || d_model % 16 != 0) return SKV_ERR_INVALID_ARG;
+    switch (head_dim) {
+        case 64: case 128: case 256: break;
+        default: return SKV_ERR_UNSUPPORTED;
+    }
+    const int64_t hd = int64_t(n_heads) * head_dim;
+    if (hd > 65536 || d_model > 65536 || Q > 0x7fffffffLL) return SKV_ERR_UNSUPPORTED;
+    if (Q == 0) return SKV_OK;
+    if (bad_ptr(o_part, 16) || bad_ptr(lse_part, 4) || bad_ptr(w_o, 16) || bad_ptr(o, 16) || bad_ptr(y, 16) ||
+        (lse && bad_ptr(lse, 4)))
+        return SKV_ERR_INVALID_ARG;
+    skv_host::Ctx c;
+    skv_status st = skv_host::get_ctx(stream, c);
+    if (st != SKV_OK) return st;
+    // Eq. 4 over the partials into o (bf16), then Eq. 5's projection of the sum
+    if ((st = skv_internal::launch_merge(o_part, lse_part, P, Q * n_heads, head_dim, o, SKV_BF16, lse, c)) != SKV_OK)
+        return st;
+    return skv_internal::launch_oproj(o, Q, (int)hd, w_o, d_model, y, c);
+}
+
 skv_status skv_lse_merge_bwd(const float* o_part, const float* lse_part, int32_t P, int64_t rows,
                              int32_t head_dim, const void* dO, skv_dtype do_dtype, const float* dlse, float* do_part,
                              float* dlse_part, void* stream) {

@@ -66,7 +66,7 @@ void note_launch(int n = 1);
 // Optional per-kernel CUDA-event timing (skv_set_kernel_timing): slots of the
 // main kernels; begin/end record events on the launching stream when enabled.
 enum TimerSlot { kTimeFwd = 0, kTimeMerge = 1, kTimeBwdKV = 2, kTimeBwdQ = 3, kTimeLocalFwd = 4, kTimeLocalBwd = 5,
-                 kTimeSlots = 6 };
+                 kTimeOproj = 6, kTimeSlots = 7 };
 void timer_begin(int slot, cudaStream_t stream);
 void timer_end(int slot, cudaStream_t stream);
 

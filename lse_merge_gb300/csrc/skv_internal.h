@@ -23,6 +23,9 @@ skv_status launch_merge(const float* o_part, const float* lse_part, int P, int64
 skv_status launch_merge_bwd(const float* o_part, const float* lse_part, int P, int64_t rows, int d, const void* dO,
                             skv_dtype do_dtype, const float* dlse, float* do_part, float* dlse_part,
                             const skv_host::Ctx& c);
+// Y = o W_o^T (tcgen05 GEMM): o bf16 [Qn][hd], w_o bf16 [d_model][hd], y fp32 [Qn][d_model]
+skv_status launch_oproj(const void* o, int64_t Qn, int hd, const void* w_o, int d_model, float* y,
+                        const skv_host::Ctx& c);
 // D_r = dO_r . o_r and lse2_r = lse_r * log2(e) (base-2 LSE for exp2 kernels);
 // row-major [Qn][H] or head-major [H][Qp] (pad rows: lse2 = +inf, D = 0)
 skv_status launch_bwd_prep(const void* o, const void* dO, const float* lse, skv_dtype dt, int64_t Qn, int64_t Qp,

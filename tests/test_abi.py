@@ -126,3 +126,22 @@ def test_python_binding_fails_loudly_without_library(tmp_path):
             _lib.load(str(tmp_path / "libskv.so"))
         finally:
             _lib._lib = saved
+
+
+def test_merge_oproj_rejects_bad_shapes_on_the_host(lib):
+    f = lib.skv_lse_merge_oproj
+    args = dict(o_part=0x1000, lse_part=0x2000, P=4, Q=128, H=4, d=128, w=0x3000, d_model=256, o=0x4000, lse=0x5000,
+                y=0x6000)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["o_part"], a["lse_part"], a["P"], a["Q"], a["H"], a["d"], a["w"], a["d_model"], a["o"], a["lse"],
+                 a["y"], None)
+
+    assert call(d_model=100) == _lib.SKV_ERR_INVALID_ARG        # not a multiple of 16
+    assert call(d_model=0) == _lib.SKV_ERR_INVALID_ARG
+    assert call(P=0) == _lib.SKV_ERR_INVALID_ARG
+    assert call(d=96) == _lib.SKV_ERR_UNSUPPORTED
+    assert call(w=0x3008) == _lib.SKV_ERR_INVALID_ARG           # misaligned weight
+    assert call(y=0) == _lib.SKV_ERR_INVALID_ARG
+    assert call(Q=0) == _lib.SKV_OK                             # nothing to do

@@ -232,3 +232,14 @@ def merge_partials(seed: int, P: int, rows: int, d: int, do_dtype: str = "fp32",
     dO = torch.randn(rows, d, generator=g, device=device).to(torch.float32 if do_dtype == "fp32" else torch.bfloat16)
     dlse = torch.randn(rows, generator=g, device=device)
     return o_part, lse_part, dO, dlse
+
+
+def oproj_weight(seed: int, d_model: int, hd: int, device: str = "cpu") -> torch.Tensor:
+    """A seeded synthetic output-projection weight W_o, bf16 [d_model, hd] (the
+    drafters' hidden sizes of Split-KV Table 2 are 2048 and 5120 over
+    32 x 128 = 4096 attention columns): N(0, 1) / sqrt(hd), so each output has
+    the scale of one attention row."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    w = torch.randn(d_model, hd, generator=g, device=device) / (hd ** 0.5)
+    return w.to(torch.bfloat16)
