@@ -1,4 +1,6 @@
-// Block-local term of the anchor mask for libskv (sm_103a, CUDA cores).
+// Block-local term of the anchor mask for libskv (sm_103a, CUDA cores): fp32
+// inputs and blocks of more than 16 rows (bf16 blocks of up to 16 rows take the
+// warp-MMA kernels of skv_block_local_mma.cu).
 //
 // [Split-KV §3.1, Fig. 1 caption] Besides its context window, each block's B
 // tokens attend bidirectionally to each other.  Those B keys/values are the
@@ -431,6 +433,7 @@ skv_status launch_block_local_fwd(const skv_problem& pb, const void* q, const vo
     skv_host::timer_begin(skv_host::kTimeLocalFwd, c.stream);
     const bool bf = pb.dtype == SKV_BF16;
     const skv_status st =
+        block_local_mma_supported(pb) ? launch_block_local_fwd_mma(pb, q, kb, vb, o, lse, c) :
         pb.head_dim == 128
             ? (bf ? fwd_rows<__nv_bfloat16, 128>(pb, q, kb, vb, o, lse, (unsigned)items, c)
                   : fwd_rows<float, 128>(pb, q, kb, vb, o, lse, (unsigned)items, c))
@@ -452,6 +455,7 @@ skv_status launch_block_local_bwd(const skv_problem& pb, const void* q, const vo
     const bool bf = pb.dtype == SKV_BF16;
     const unsigned n = (unsigned)items;
     const skv_status st =
+        block_local_mma_supported(pb) ? launch_block_local_bwd_mma(pb, q, kb, vb, o, lse, dO, dq, dkb, dvb, c) :
         pb.head_dim == 128
             ? (bf ? bwd_rows<__nv_bfloat16, 128>(pb, q, kb, vb, o, lse, dO, dq, dkb, dvb, n, c)
                   : bwd_rows<float, 128>(pb, q, kb, vb, o, lse, dO, dq, dkb, dvb, n, c))

@@ -42,6 +42,13 @@ skv_status launch_attn_bwd_simt(const skv_problem& pb, const void* q, const void
                                 const void* dO, const float* lse, const float* D, skv::RankCSR csr,
                                 float* dq_part, float* dk, float* dv, const skv_host::Ctx& c);
 
+// block-local term on warp-level MMA (bf16, B <= 16, head_dim 64 or 128)
+bool block_local_mma_supported(const skv_problem& pb);
+skv_status launch_block_local_fwd_mma(const skv_problem& pb, const void* q, const void* kb, const void* vb, float* o,
+                                      float* lse, const skv_host::Ctx& c);
+skv_status launch_block_local_bwd_mma(const skv_problem& pb, const void* q, const void* kb, const void* vb,
+                                      const void* o, const float* lse, const void* dO, float* dq, float* dkb,
+                                      float* dvb, const skv_host::Ctx& c);
 // block-local term of the mask (each block over its own B keys), CUDA cores
 bool block_local_supported(const skv_problem& pb);
 skv_status launch_block_local_fwd(const skv_problem& pb, const void* q, const void* kb, const void* vb, float* o,
