@@ -174,13 +174,15 @@ SKV_API skv_status skv_attn_fwd(const skv_problem* prob, const void* q, const vo
  *
  * Same arguments, semantics and outputs as skv_attn_fwd.  The scratch the
  * forward needs (the per-rank chunk lists, 4 bytes per chunk and per rank, and
- * the key bounds of each 128-row query tile, 16 bytes each, counted only for
- * bf16 problems, whose tensor-core forward uses them) lives in a fixed
- * 128 KiB array in device memory that every GPU loading the library holds
- * until the process exits; the call itself allocates nothing.  Problems whose
- * forward workspace (skv_workspace_bytes(prob, 0)) exceeds 131072 bytes are
- * rejected with SKV_ERR_WORKSPACE before any launch -- e.g. 16384 chunks over
- * 1024 ranks with up to 3800 query tiles (Q <= 486 400 rows) fit.
+ * the key bounds of each query tile, 16 bytes each, counted only for bf16
+ * problems, whose tensor-core forward uses them; a tile is 128 query rows, or
+ * 128/g rows of each of the g query heads of a key/value head with grouped
+ * queries) lives in a fixed 128 KiB array in device memory that every GPU
+ * loading the library holds until the process exits; the call itself
+ * allocates nothing.  Problems whose forward workspace
+ * (skv_workspace_bytes(prob, 0)) exceeds 131072 bytes are rejected with
+ * SKV_ERR_WORKSPACE before any launch -- e.g. 16384 chunks over 1024 ranks
+ * with up to 3800 query tiles (Q <= 486 400 rows without grouped queries) fit.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream

@@ -24,7 +24,9 @@
 //    in TMEM as A operands; per key tile:
 //      S = Q K^T, dP = dO V^T (TS); eight warps form dS (bf16 -> TMEM over the
 //      dP they read); dQ += dS K (TS).  S of the next tile is issued as soon as
-//      S has been read, so it overlaps the forming of P and dS.
+//      S has been read, so it overlaps the forming of P and dS.  With grouped
+//      queries the tile stacks the group's g query heads (128/g rows each), as
+//      in the forward, so each K/V tile is loaded once per group.
 // Recomputing S and dP in the second kernel costs two extra GEMMs per tile pair
 // but removes every dq reduction from the key-stationary loop.
 #include <cuda.h>
@@ -53,10 +55,10 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 
 // Per query tile: union (lo, hi) and full-visibility (flo, fhi) key bounds.
 __global__ void qtile_bounds_kernel(const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int64_t Qn,
-                                    int64_t S, int n_qt, int4* __restrict__ out) {
+                                    int64_t S, int n_qt, int4* __restrict__ out, int rows) {
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= n_qt) return;
-    const TileBounds tb = tile_bounds(s, a, B, Qn, S, t);
+    const TileBounds tb = tile_bounds(s, a, B, Qn, S, t, rows);
     out[t] = make_int4((int)tb.lo, (int)tb.hi, (int)tb.flo, (int)tb.fhi);
 }
 
@@ -595,7 +597,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_co
                       const float* __restrict__ lse2_hm, const float* __restrict__ D_hm, int64_t Qp,
                       const int32_t* __restrict__ s, const int32_t* __restrict__ a, int B, int64_t Qn, int H,
                       int gq, int64_t S, int m, int P, float scale, float scale_log2, const int4* __restrict__ qtb,
-                      skv::RankCSR csr, float* __restrict__ dq, int* status, long long wait_limit) {
+                      int pk, skv::RankCSR csr, float* __restrict__ dq, int* status, long long wait_limit) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t base_s = smem_u32(smem_raw);
     const uint32_t pad = ((base_s + 1023u) & ~1023u) - base_s;
@@ -609,8 +611,12 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_co
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // query tiles in descending order: the last tiles of a sample see the longest
     // windows, so the longest blocks start first and the grid's tail is short ones
-    const int qt = gridDim.x - 1 - blockIdx.x, h = blockIdx.y;
-    const int kvh = h / gq;                          // key/value head of this query head
+    // A tile holds pk query heads (the group of one key/value head when pk > 1), each
+    // over R = 128/pk query rows: tile row r is query row qt*R + r % R of head
+    // h0 + r / R, so the group's heads share every K/V tile.
+    const int qt = gridDim.x - 1 - blockIdx.x, h0 = blockIdx.y * pk;
+    const int R = BM / pk;
+    const int kvh = h0 / gq;                         // key/value head of these query heads
     constexpr int NP = D / 64;
     constexpr uint32_t kTile = BM * D * 2;
     const bool stuck_test = wait_limit < 0;
@@ -788,7 +794,8 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_co
         const int quad = warp & 3, hf = warp >> 2;
         const uint32_t lane_base = uint32_t(quad * 32) << 16;
         const int r = quad * 32 + lane;
-        const int64_t row = int64_t(qt) * BM + r;
+        const int64_t row = int64_t(qt) * R + r % R;
+        const int h = h0 + r / R;                        // this row's query head
         const bool live = row < Qn;
         int64_t rlo = 0, rhi = 0;
         if (live) skv::block_window(s, a, (int)(row / B), S, rlo, rhi);
@@ -923,9 +930,10 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_co
 // ============================================================== host side
 
 struct BwdScratch {
-    int4* qtb;
+    int4* qtb;          // per 128-row query tile
     int32_t* cnt;
     int32_t* list;
+    int4* gtb;          // per tile of the dQ kernel (stacked heads), or qtb
 };
 
 size_t scratch_layout(const skv_problem& pb, BwdScratch* w, char* base) {
@@ -937,10 +945,15 @@ size_t scratch_layout(const skv_problem& pb, BwdScratch* w, char* base) {
     const size_t o_qtb = off; off = align256(off + size_t(n_qt) * sizeof(int4));
     const size_t o_cnt = off; off = align256(off + size_t(n_kv) * 4);
     const size_t o_list = off; off = align256(off + size_t(n_kv) * size_t(n_qt) * 4);
+    // key bounds of the dQ kernel's tiles when they stack a group's query heads
+    const int pk = skv_tc::pack_heads(pb);
+    const int64_t n_gt = pk > 1 ? (Qn + BM / pk - 1) / (BM / pk) : 0;
+    const size_t o_gtb = off; off = align256(off + size_t(n_gt) * sizeof(int4));
     if (w) {
         w->qtb = reinterpret_cast<int4*>(base + o_qtb);
         w->cnt = reinterpret_cast<int32_t*>(base + o_cnt);
         w->list = reinterpret_cast<int32_t*>(base + o_list);
+        w->gtb = pk > 1 ? reinterpret_cast<int4*>(base + o_gtb) : w->qtb;
     }
     return off;
 }
@@ -955,10 +968,16 @@ skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const
     const int n_kv = (int)(pb.S / BN);
     BwdScratch w;
     scratch_layout(pb, &w, static_cast<char*>(scratch));
-    qtile_bounds_kernel<<<(n_qt + 127) / 128, 128, 0, c.stream>>>(pb.s, pb.a, pb.B, Qn, pb.S, n_qt, w.qtb);
+    qtile_bounds_kernel<<<(n_qt + 127) / 128, 128, 0, c.stream>>>(pb.s, pb.a, pb.B, Qn, pb.S, n_qt, w.qtb, BM);
     SKV_LAUNCHED();
     kv_list_kernel<<<(n_kv + 7) / 8, 256, 0, c.stream>>>(w.qtb, n_qt, n_kv, w.cnt, w.list);
     SKV_LAUNCHED();
+    const int pk = skv_tc::pack_heads(pb), R = BM / pk;
+    const int n_gt = (int)((Qn + R - 1) / R);
+    if (pk > 1) {
+        qtile_bounds_kernel<<<(n_gt + 127) / 128, 128, 0, c.stream>>>(pb.s, pb.a, pb.B, Qn, pb.S, n_gt, w.gtb, R);
+        SKV_LAUNCHED();
+    }
     CUtensorMap mq, mdo, mk, mv, mdk, mdv;
     const int64_t cols = int64_t(pb.n_heads) * D, kv_cols = int64_t(pb.n_kv_heads) * D;
     const int gq = pb.n_heads / pb.n_kv_heads;
@@ -981,9 +1000,9 @@ skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const
         auto kern = attn_bwd_dq_tc_kernel<D>;
         SKV_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax));
         skv_host::timer_begin(skv_host::kTimeBwdQ, c.stream);
-        kern<<<dim3((unsigned)n_qt, (unsigned)pb.n_heads), kQThreads, kSmemMax, c.stream>>>(
+        kern<<<dim3((unsigned)n_gt, (unsigned)(pb.n_heads / pk)), kQThreads, kSmemMax, c.stream>>>(
             mk, mv, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(dO), lse2_hm, D_hm, Qp,
-            pb.s, pb.a, pb.B, Qn, pb.n_heads, gq, pb.S, pb.m, pb.P, pb.scale, scale_log2, w.qtb, csr, dq,
+            pb.s, pb.a, pb.B, Qn, pb.n_heads, gq, pb.S, pb.m, pb.P, pb.scale, scale_log2, w.gtb, pk, csr, dq,
             c.status, c.wait_limit);
         skv_host::timer_end(skv_host::kTimeBwdQ, c.stream);
         SKV_LAUNCHED();
@@ -995,11 +1014,12 @@ skv_status launch_bwd(const skv_problem& pb, const void* q, const void* k, const
 
 namespace skv_tc {
 
-skv_status launch_qtile_bounds(const skv_problem& pb, int4* out, const skv_host::Ctx& c) {
+skv_status launch_qtile_bounds(const skv_problem& pb, int4* out, const skv_host::Ctx& c, int rows) {
     const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
-    const int64_t n_qt = (Qn + BM - 1) / BM;
+    const int64_t n_qt = (Qn + rows - 1) / rows;
     if (n_qt == 0) return SKV_OK;
-    qtile_bounds_kernel<<<(unsigned)((n_qt + 127) / 128), 128, 0, c.stream>>>(pb.s, pb.a, pb.B, Qn, pb.S, (int)n_qt, out);
+    qtile_bounds_kernel<<<(unsigned)((n_qt + 127) / 128), 128, 0, c.stream>>>(pb.s, pb.a, pb.B, Qn, pb.S, (int)n_qt, out,
+                                                                            rows);
     SKV_LAUNCHED();
     return SKV_OK;
 }

@@ -8,6 +8,12 @@
 // chunks that intersect the union of its rows' windows [s_i, a_i) (§3.1
 // Fig. 1); every other tile is never loaded.  Tiles inside every row's window
 // are processed unmasked; only boundary tiles get the per-row compare.
+// Grouped-query layouts [Split-KV Table 2] stack the g query heads of one
+// key/value head in a tile, 128/g rows each (row r of the tile is query row
+// r % (128/g) of the tile's row range, head r / (128/g) of the group): one K/V
+// tile then serves the whole group, and a tile's rows come from g times fewer
+// blocks, so fewer of its key tiles are boundary tiles.  A rank whose chunks
+// miss both tiles' windows only marks their rows empty.
 //
 // The two query tiles share every K/V tile and alternate on the tensor core,
 // so one tile's exponentials overlap the other tile's MMAs.  Roles (320 threads):
@@ -66,15 +72,19 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
                    const int32_t* __restrict__ s,
                    const int32_t* __restrict__ a, int B, int64_t Qn, int H, int gq, int64_t S, int m,
-                   float scale_log2, skv::RankCSR csr, const int4* __restrict__ qtb, int n_qt,
+                   float scale_log2, skv::RankCSR csr, const int4* __restrict__ qtb, int n_qt, int pk,
                    float* __restrict__ o_part, float* __restrict__ lse_part, int* status, long long wait_limit) {
     extern __shared__ unsigned char smem_raw[];
     FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // query tile pairs in descending order: the last tiles of a sample see the longest
-    // windows, so the longest blocks start first and each head's tail is short ones
-    const int qt0 = 2 * (gridDim.x - 1 - blockIdx.x), h = blockIdx.y, p = blockIdx.z;
-    const int kvh = h / gq;                          // key/value head of this query head
+    // windows, so the longest blocks start first and each head's tail is short ones.
+    // A tile holds pk query heads (the group of one key/value head when pk > 1), each
+    // over R = 128/pk query rows: tile row r is query row qt*R + r % R of head
+    // h0 + r / R, so the group's heads share every K/V tile.
+    const int qt0 = 2 * (gridDim.x - 1 - blockIdx.x), h0 = blockIdx.y * pk, p = blockIdx.z;
+    const int R = BM / pk;
+    const int kvh = h0 / gq;                         // key/value head of these query heads
     constexpr int NP = D / 64;                       // 64-column panels per row
     constexpr uint32_t kTileBytes = BN * D * 2;      // one K or V tile (== Q tile)
 
@@ -91,6 +101,21 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     // once any block of the launch has timed out the result is void: the
     // remaining blocks skip their work instead of each waiting out a deadline
     if (*(volatile int*)status == SKV_ERR_TIMEOUT) hi = lo;
+    // a rank holding no key of the two tiles' windows (half of all blocks when a
+    // rank keeps one chunk of each sample) only marks the tiles' rows empty:
+    // lse_part = -inf, o_part unspecified; no barriers, no TMEM
+    {
+        TileIter probe;
+        probe.init(csr, p, p + 1, m, lo, hi);
+        if (probe.count() == 0) {
+            if (warp < 8) {
+                const int r = (warp & 3) * 32 + lane;
+                const int64_t row = int64_t(qt0 + (warp >> 2)) * R + r % R;
+                if (row < Qn) lse_part[(int64_t(p) * Qn + row) * H + h0 + r / R] = -INFINITY;
+            }
+            return;
+        }
+    }
 
     if (tid == 0) {
         mbar_init(&sm.q_full, 1);
@@ -142,7 +167,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         const int j = warp >> 2;                       // query tile of this warpgroup
         const int quad = warp & 3;
         const int r = quad * 32 + lane;                // row inside the tile == TMEM lane
-        const int64_t row = int64_t(qt0 + j) * BM + r;
+        const int64_t row = int64_t(qt0 + j) * R + r % R;
+        const int h = h0 + r / R;                      // this row's query head
         const bool live = row < Qn;
         // positions fit in int32 here (anchors are int32 and S < 2^31 on this path)
         int rlo = 0, rhi = 0;
@@ -277,10 +303,13 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
+                    // boxes of min(R, 32) rows, each inside one head's rows
+                    const int BR = R < 32 ? R : 32;
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c)
-                        tma_store_3d(&map_o, stage + c * (BM * 128) + quad * 32 * 128, h * D + c * 32,
-                                     (qt0 + j) * BM + quad * 32, p);
+                        for (int rr = quad * 32; rr < quad * 32 + 32; rr += BR)
+                            tma_store_3d(&map_o, stage + c * (BM * 128) + rr * 128, (h0 + rr / R) * D + c * 32,
+                                         (qt0 + j) * R + rr % R, p);
                     bulk_commit_group();
                     bulk_wait_read_all();
                 }
@@ -303,9 +332,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                         prefetch_tensormap(&map_k);
                         prefetch_tensormap(&map_v);
                         mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
+                        // tile j: rows [k R, k R + R) of each panel from head h0 + k
                         for (int j = 0; j < 2; ++j)
-                            for (int c = 0; c < NP; ++c)
-                                tma_load_2d(sm.q[j][c], &map_q, &sm.q_full, h * D + c * 64, (qt0 + j) * BM);
+                            for (int k = 0; k < pk; ++k)
+                                for (int c = 0; c < NP; ++c)
+                                    tma_load_2d(&sm.q[j][c][k * R * 64], &map_q, &sm.q_full, (h0 + k) * D + c * 64,
+                                                (qt0 + j) * R);
                         any = true;
                     }
                     const int st = n % kStages;
@@ -414,10 +446,11 @@ template <int D>
 skv_status launch_fwd(const skv_problem& pb, const void* q, const void* k, const void* v, skv::RankCSR csr,
                       float* o_part, float* lse_part, void* scratch, const skv_host::Ctx& c) {
     const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
+    const int pk = skv_tc::pack_heads(pb), R = BM / pk;
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, q, Qn, int64_t(pb.n_heads) * D) || !make_map(&mk, k, pb.S, int64_t(pb.n_kv_heads) * D) ||
+    if (!make_map(&mq, q, Qn, int64_t(pb.n_heads) * D, R) || !make_map(&mk, k, pb.S, int64_t(pb.n_kv_heads) * D) ||
         !make_map(&mv, v, pb.S, int64_t(pb.n_kv_heads) * D) ||
-        !make_map_f32_3d(&mo, o_part, pb.P, Qn, int64_t(pb.n_heads) * D))
+        !make_map_f32_3d(&mo, o_part, pb.P, Qn, int64_t(pb.n_heads) * D, R < 32 ? R : 32))
         return SKV_ERR_CUDA;
     size_t smem = sizeof(FwdSmem<D>) + 1024;
     if (smem < 120 * 1024) smem = 120 * 1024;   // one block per SM: it owns all 512 TMEM columns
@@ -428,16 +461,16 @@ skv_status launch_fwd(const skv_problem& pb, const void* q, const void* k, const
     cudaFuncAttributes fa;
     SKV_CUDA_CHECK(cudaFuncGetAttributes(&fa, kern));
     if (fa.numRegs * kFwdThreads < 2 * 128 * kRegSoftmax + 128 * kRegIssue) return SKV_ERR_UNSUPPORTED;
-    const int64_t n_qt = (Qn + BM - 1) / BM;
+    const int64_t n_qt = (Qn + R - 1) / R;               // tiles of R rows x pk heads
     int4* qtb = static_cast<int4*>(scratch);
-    skv_status st = skv_tc::launch_qtile_bounds(pb, qtb, c);
+    skv_status st = skv_tc::launch_qtile_bounds(pb, qtb, c, R);
     if (st != SKV_OK) return st;
-    const dim3 grid((unsigned)((n_qt + 1) / 2), (unsigned)pb.n_heads, (unsigned)pb.P);
+    const dim3 grid((unsigned)((n_qt + 1) / 2), (unsigned)(pb.n_heads / pk), (unsigned)pb.P);
     const float scale_log2 = pb.scale * 1.4426950408889634f;
     skv_host::timer_begin(skv_host::kTimeFwd, c.stream);
     kern<<<grid, kFwdThreads, smem, c.stream>>>(mq, mk, mv, mo, pb.s, pb.a, pb.B, Qn, pb.n_heads,
                                                 pb.n_heads / pb.n_kv_heads, pb.S, pb.m, scale_log2,
-                                                csr, qtb, (int)n_qt, o_part, lse_part, c.status, c.wait_limit);
+                                                csr, qtb, (int)n_qt, pk, o_part, lse_part, c.status, c.wait_limit);
     skv_host::timer_end(skv_host::kTimeFwd, c.stream);
     SKV_LAUNCHED();
     return SKV_OK;
@@ -455,7 +488,8 @@ bool fwd_supported(const skv_problem& pb) {
 size_t fwd_scratch_bytes(const skv_problem& pb) {   // per query tile key bounds (int4); none off this path
     if (!fwd_supported(pb)) return 0;
     const int64_t Qn = int64_t(pb.n_blocks) * pb.B;
-    return size_t((Qn + BM - 1) / BM) * sizeof(int4);
+    const int R = BM / pack_heads(pb);
+    return size_t((Qn + R - 1) / R) * sizeof(int4);
 }
 
 skv_status launch_attn_fwd_tc(const skv_problem& pb, const void* q, const void* k, const void* v, skv::RankCSR csr,

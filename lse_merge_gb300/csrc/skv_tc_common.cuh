@@ -11,17 +11,18 @@ namespace skv_tcc {
 constexpr int BM = 128;          // query rows per tile
 constexpr int BN = 128;          // keys per tile
 
-// Rows [qt*128, qt*128+128) of the packed query: tile-level key bounds.
+// Rows [qt*rows, qt*rows+rows) of the packed query (rows = 128 for a plain tile,
+// 128/g when a tile stacks the g query heads of a key/value head): key bounds.
 struct TileBounds {
     int64_t lo, hi;     // union of the rows' windows (empty if lo >= hi)
     int64_t flo, fhi;   // intersection: keys every live row sees
 };
 
 __device__ __forceinline__ TileBounds tile_bounds(const int32_t* s, const int32_t* a, int B, int64_t Qn, int64_t S,
-                                                  int qt) {
+                                                  int qt, int rows = BM) {
     TileBounds tb{S, 0, 0, S};
-    const int64_t r0 = int64_t(qt) * BM;
-    const int64_t r1 = (r0 + BM < Qn ? r0 + BM : Qn) - 1;
+    const int64_t r0 = int64_t(qt) * rows;
+    const int64_t r1 = (r0 + rows < Qn ? r0 + rows : Qn) - 1;
     bool any_empty = false;
     for (int64_t i = r0 / B; i <= r1 / B; ++i) {
         int64_t lo, hi;
@@ -35,7 +36,7 @@ __device__ __forceinline__ TileBounds tile_bounds(const int32_t* s, const int32_
         tb.flo = lo > tb.flo ? lo : tb.flo;
         tb.fhi = hi < tb.fhi ? hi : tb.fhi;
     }
-    if (any_empty || r1 - r0 + 1 < BM) tb.fhi = tb.flo;   // partial or empty rows: mask every tile
+    if (any_empty || r1 - r0 + 1 < rows) tb.fhi = tb.flo;   // partial or empty rows: mask every tile
     return tb;
 }
 
@@ -102,13 +103,13 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2D bf16 view [rows][cols] of a row-major tensor, 64x128 boxes, 128-byte swizzle.
-inline bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols) {
+// 2D bf16 view [rows][cols] of a row-major tensor, 64 x box_rows boxes, 128-byte swizzle.
+inline bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows = 128) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, 128};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -128,14 +129,14 @@ inline bool make_map_f32(CUtensorMap* map, void* ptr, int64_t rows, int64_t cols
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-// 3D fp32 view [d2][d1][cols] of a row-major tensor, 32x32x1 boxes, 128-byte
+// 3D fp32 view [d2][d1][cols] of a row-major tensor, 32 x box_rows x 1 boxes, 128-byte
 // swizzle: rows past d1 inside one d2 slice are dropped by a store.
-inline bool make_map_f32_3d(CUtensorMap* map, void* ptr, int64_t d2, int64_t d1, int64_t cols) {
+inline bool make_map_f32_3d(CUtensorMap* map, void* ptr, int64_t d2, int64_t d1, int64_t cols, int box_rows = 32) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)d1, (cuuint64_t)d2};
     cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)(cols * d1) * 4};
-    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -2,6 +2,8 @@
 times: the oracle computes sampled outputs one query block / key at a time
 (two heads, 0 and H-1), and properties that hold at any size are checked on
 every output (the exact -inf pattern of the partials, finiteness)."""
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -48,8 +50,13 @@ def full_run(request):
     o, lse = skv.lse_merge(o_part, lse_part, out_dtype=torch.bfloat16)
     dq, dk, dv = skv.attn_bwd(prob, inp.q, inp.k, inp.v, o, lse, inp.dO, roc)
     assert skv.stream_status() == 0
-    yield w, inp, prob, roc.cpu().numpy(), o_part, lse_part, o, lse, dq, dk, dv
-    del o_part, lse_part, dq, dk, dv
+    # a list, emptied at teardown: whatever still holds it then no longer holds the
+    # workload's ~140 GB of device tensors when the next workload is drawn
+    run = [w, inp, prob, roc.cpu().numpy(), o_part, lse_part, o, lse, dq, dk, dv]
+    yield run
+    run.clear()
+    del inp, prob, o_part, lse_part, o, lse, dq, dk, dv, s, a, costs, roc
+    gc.collect()
     torch.cuda.empty_cache()
 
 

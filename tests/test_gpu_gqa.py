@@ -1,7 +1,9 @@
 """GPU parity of the grouped-query layouts [Split-KV Table 2: 32 query heads
 over 4 or 8 key/value heads] against the CPU fp64 oracle on the same seeded
 inputs: query head h reads key/value head h // (H / Hkv), and dk, dv (and the
-block-local dk_blk, dv_blk) sum over each key/value head's query heads.
+block-local dk_blk, dv_blk) sum over each key/value head's query heads.  The
+tensor-core forward and dQ kernels stack a group's g query heads in one
+128-row tile (128/g rows each); the cases cover g = 2, 4, 8 and 16.
 Element by element at sizes the oracle finishes in seconds (tensor-core bf16
 and CUDA-core fp32 paths, multi-query Hkv = 1, ragged B); the full packed
 shape with Hkv = 8 runs in tests/test_gpu_full.py.  Tolerances as for the
@@ -24,6 +26,7 @@ pytestmark = pytest.mark.gpu
     (42, 1, 1408, 9, 16, 8, 1, 128, 128, 11, "bf16", "contiguous"),  # one key/value head
     (43, 2, 768, 5, 5, 4, 2, 64, 128, 3, "fp32", "lpt"),             # CUDA-core path, ragged B
     (44, 1, 640, 4, 24, 6, 3, 64, 128, 5, "bf16", "lpt"),            # B > 16, groups of 2
+    (48, 1, 1024, 9, 16, 16, 1, 128, 256, 4, "bf16", "lpt"),         # 16 heads a tile, 8 rows each
 ])
 def test_gqa_forward_backward(cfg):
     seed, b, L, A, B, H, Hkv, dd, m, P, dt, order = cfg
