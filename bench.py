@@ -425,6 +425,37 @@ def run_ours(args):
     ms = slowest([ms], world, dev)[0]
     if skv.stream_status() != 0:
         raise RuntimeError("device status set during the timed region")
+    # a short step is bound by its launches: the same step captured once in a CUDA
+    # graph and replayed (its own pass, reported beside the eager number)
+    graph = None
+    if ms < 20.0 and world == 1:
+        try:
+            gr = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                path()                                  # warm the allocations of the captured stream
+            torch.cuda.current_stream(dev).wait_stream(side)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(gr, capture_error_mode="thread_local"):
+                path()
+            gr.replay()
+            torch.cuda.synchronize()
+            g_s, g_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g_s.record()
+            for _ in range(args.steps):
+                gr.replay()
+            g_e.record()
+            torch.cuda.synchronize()
+            if skv.stream_status() != 0:
+                raise RuntimeError("device status set by the graph replays")
+            g_ms = g_s.elapsed_time(g_e) / args.steps
+            graph = {"ms_per_step": g_ms, "value": job_tflops(4.0 * d * useful_pairs_per_head(inp.s, inp.a, w.B) * H
+                                                             * (3.0 if w.backward else 1.0), world, g_ms),
+                     "mode": "the whole step captured once in a CUDA graph and replayed"}
+            del gr
+        except Exception as exc:                        # reported, never fatal
+            graph = {"error": f"{type(exc).__name__}: {exc}"[:200]}
     # per-kernel durations: the library's own CUDA events on the launching
     # stream, read after each step of a separate pass of the same steps
     kt_ms = [[] for _ in kt_names]
@@ -547,15 +578,17 @@ def run_ours(args):
     tensor_k = {k: v for k, v in kernels.items() if k in credit}
     dom = max(tensor_k, key=lambda k: tensor_k[k]["ms"]) if tensor_k else None
     dom_tf = tensor_k[dom]["useful_tflops"] if dom else 0.0
+    # DRAM bytes of one launch of the dominant kernel, read with ncu on this very
+    # workload (profiles/traffic.json); null for a workload without a capture, and
+    # once the kernels differ from the ones the counters were taken on
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
     if dom and os.path.exists(tr_path):
         with open(tr_path) as f:
             tr = json.load(f)
-        per_pair = tr.get(dom, {}).get("dram_bytes_per_useful_pair_head")
-        # null once the kernels differ from the ones the counters were taken on
-        if per_pair and tr.get("csrc_sha256") == csrc_digest():
-            traffic = per_pair * pairs
+        per_launch = tr.get("per_launch", {}).get(w.name, {}).get(dom, {}).get("dram_bytes")
+        if per_launch and tr.get("csrc_sha256") == csrc_digest():
+            traffic = per_launch
 
     # the CPU baseline before the end-to-end pass: the pinned host buffers of the
     # largest workloads and the oracle's arrays do not fit in host memory together
@@ -711,6 +744,7 @@ def run_ours(args):
                                route="per-partial MERGE_BWD on this step's partials (own pass)")
                           if mbwd else None),
             "gpu_launches": int(launches),
+            "cuda_graph": graph,
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -18,9 +18,10 @@
 //      of dS^T; then S of the next tile; dK += dS^T Q_t (TS); dP of the next tile.
 //    dK and dV leave through shared memory with TMA stores.
 //  * attn_bwd_dq_tc_kernel -- query-stationary.  One thread block owns a
-//    128-row query tile and a head and walks, rank by rank, the key tiles of
-//    every rank's chunks that meet the tile's windows: dq = sum_p dq^(p)
-//    (Alg. 1's dq reduce-scatter) is accumulated in TMEM and written once.  Q and dO stay
+//    128-row query tile and a head and walks the key tiles that meet the tile's
+//    windows, in ascending order: dq = sum_p dq^(p) (Alg. 1's dq reduce-scatter),
+//    whose ranks' chunks tile the keys exactly, is accumulated in TMEM over all of
+//    them and written once.  Q and dO stay
 //    in TMEM as A operands; per key tile:
 //      S = Q K^T, dP = dO V^T (TS); eight warps form dS (bf16 -> TMEM over the
 //      dP they read); dQ += dS K (TS).  S of the next tile is issued as soon as
@@ -623,8 +624,11 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_co
     if (stuck_test) wait_limit = -wait_limit;
     int4 bnd = qtb[qt];
     if (*(volatile int*)status == SKV_ERR_TIMEOUT) bnd.y = bnd.x;   // launch already void: no tiles
-    TileIter it;
-    it.init(csr, 0, P, m, bnd.x, bnd.y);             // every rank's chunks: dq = sum_p dq^(p)
+    // dq = sum_p dq^(p) over every rank's chunks: on one device that is the sum over
+    // every key of the tile's windows, walked in ascending order (the ranks' chunks
+    // tile [0, S) exactly, so the order changes only the fp32 rounding)
+    KeyRange it;
+    it.init(bnd.x, bnd.y);
 
     if (tid == 0) {
         for (int i = 0; i < kKStages; ++i) {

@@ -24,7 +24,7 @@ namespace {
 constexpr unsigned kAll = 0xffffffffu;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kWarpsFwd = 4, kWarpsBwd = 4;
+constexpr int kWarpsFwd = 4, kWarpsBwd = 2;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -202,10 +202,12 @@ block_local_fwd_mma_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
     }
 }
 
-// dq rows g, g + 8 of head h, columns [C0, C0 + D/2): += scale dS K
+// dq rows g, g + 8 of head h, columns [C0, C0 + D/2): += scale dS K, the values added
+// to read from their staged copy sdq (fp32 rows of D + 4)
 template <int D, int C0>
-__device__ __forceinline__ void dq_add(float* __restrict__ dq, const uint32_t (&da)[4], const __nv_bfloat16* sk,
-                                       int64_t row0, int B, int H, int h, float scale, int lane) {
+__device__ __forceinline__ void dq_add(float* __restrict__ dq, const float* sdq, const uint32_t (&da)[4],
+                                       const __nv_bfloat16* sk, int64_t row0, int B, int H, int h, float scale,
+                                       int lane) {
     constexpr int NT = D / 16;
     const int g = lane >> 2, c = lane & 3;
     float acc[NT][4];
@@ -219,14 +221,22 @@ __device__ __forceinline__ void dq_add(float* __restrict__ dq, const uint32_t (&
         const int r = g + 8 * e;
         if (r < B) {
             float* dst = dq + ((row0 + r) * H + h) * D + C0 + 2 * c;
+            const float* src = sdq + r * (D + 4) + C0 + 2 * c;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float2* p2 = reinterpret_cast<float2*>(dst + nt * 8);
-                const float2 old = *p2;
-                *p2 = make_float2(fmaf(scale, acc[nt][2 * e], old.x), fmaf(scale, acc[nt][2 * e + 1], old.y));
+                const float2 old = *reinterpret_cast<const float2*>(src + nt * 8);
+                *reinterpret_cast<float2*>(dst + nt * 8) =
+                    make_float2(fmaf(scale, acc[nt][2 * e], old.x), fmaf(scale, acc[nt][2 * e + 1], old.y));
             }
         }
     }
+}
+
+// shared bytes of one backward warp: five bf16 row tiles (16 x (D + 8)), P and dS
+// (16 x 24 bf16 each), the fp32 dq rows (16 x (D + 4)); a multiple of 16
+template <int D>
+constexpr int bwd_warp_bytes() {
+    return (5 * 16 * (D + 8) + 2 * 16 * 24) * 2 + 16 * (D + 4) * 4;
 }
 
 // dq += the block-local part; dk_blk, dv_blk written.  One warp per (block,
@@ -247,14 +257,16 @@ block_local_bwd_mma_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
     if (item >= items) return;
     const int64_t i = item / Hkv;
     const int kvh = int(item % Hkv), gq = H / Hkv;
-    // per warp: k, v, q, dO, o rows, then the bf16 16 x 16 P and dS tiles
-    __nv_bfloat16* sk = reinterpret_cast<__nv_bfloat16*>(smem_raw) + warp * (5 * 16 * LD + 2 * 16 * 24);
+    // per warp: k, v, q, dO, o rows, the bf16 16 x 16 P and dS tiles, then the fp32 dq
+    // rows the block-local part is added to
+    __nv_bfloat16* sk = reinterpret_cast<__nv_bfloat16*>(smem_raw + warp * bwd_warp_bytes<D>());
     __nv_bfloat16* sv = sk + 16 * LD;
     __nv_bfloat16* sq = sv + 16 * LD;
     __nv_bfloat16* sg = sq + 16 * LD;
     __nv_bfloat16* so = sg + 16 * LD;
     __nv_bfloat16* sp = so + 16 * LD;        // P, row-major [16][24]
     __nv_bfloat16* ss = sp + 16 * 24;        // dS
+    float* sdq = reinterpret_cast<float*>(ss + 16 * 24);   // [16][D + 4]
     const int64_t row0 = i * B;
     const float scale_log2 = scale * kLog2e;
     const int g = lane >> 2, c = lane & 3;
@@ -273,6 +285,12 @@ block_local_bwd_mma_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
         stage_rows<D>(sq, q, row0, B, H, h, lane);
         stage_rows<D>(sg, dO, row0, B, H, h, lane);
         stage_rows<D>(so, o, row0, B, H, h, lane);
+        // the dq rows this head's part is added to, fetched with the inputs
+#pragma unroll 4
+        for (int e = lane; e < 16 * (D / 4); e += 32) {
+            const int r = e / (D / 4), c4 = (e % (D / 4)) * 4;
+            if (r < B) cp_async16(sdq + r * (D + 4) + c4, dq + ((row0 + r) * H + h) * D + c4);
+        }
         float l2[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -312,8 +330,8 @@ block_local_bwd_mma_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
         as_a(pa, s);
         as_a(da, dp);
         // dq rows g, g + 8 of head h: += scale dS K, in two halves of the columns
-        dq_add<D, 0>(dq, da, sk, row0, B, H, h, scale, lane);
-        dq_add<D, D / 2>(dq, da, sk, row0, B, H, h, scale, lane);
+        dq_add<D, 0>(dq, sdq, da, sk, row0, B, H, h, scale, lane);
+        dq_add<D, D / 2>(dq, sdq, da, sk, row0, B, H, h, scale, lane);
         // P and dS through shared memory (row-major bf16), read back transposed as
         // the A fragments of P^T and dS^T
 #pragma unroll
@@ -368,7 +386,7 @@ template <int D>
 skv_status bwd_go(const skv_problem& pb, const void* q, const void* kb, const void* vb, const void* o,
                   const float* lse, const void* dO, float* dq, float* dkb, float* dvb, int64_t items,
                   const skv_host::Ctx& c) {
-    const int smem = kWarpsBwd * (5 * 16 * (D + 8) + 2 * 16 * 24) * 2;
+    const int smem = kWarpsBwd * bwd_warp_bytes<D>();
     const int64_t grid = (items + kWarpsBwd - 1) / kWarpsBwd;
     if (grid > 0x7fffffffLL) return SKV_ERR_UNSUPPORTED;
     auto kern = block_local_bwd_mma_kernel<D>;

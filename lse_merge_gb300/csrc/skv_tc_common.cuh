@@ -89,6 +89,22 @@ struct TileIter {
     }
 };
 
+// The 128-key tiles that meet [lo, hi), ascending: the same interface as TileIter
+// for a walk that does not go chunk by chunk.
+struct KeyRange {
+    int64_t x, xe;
+    __device__ __forceinline__ void init(int64_t lo, int64_t hi) {
+        x = lo & ~int64_t(BN - 1);
+        xe = hi > lo ? hi : x;
+    }
+    __device__ __forceinline__ int count() const { return xe > x ? (int)((xe - x + BN - 1) / BN) : 0; }
+    __device__ __forceinline__ bool next(int64_t& x0) {
+        if (x >= xe) return false;
+        x0 = x;
+        x += BN;
+        return true;
+    }
+};
 
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
