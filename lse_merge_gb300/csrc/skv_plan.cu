@@ -51,12 +51,12 @@ __device__ __forceinline__ bool lpt_before(int64_t ca, int32_t ia, int64_t cb, i
 }
 
 constexpr int kLptThreads = 1024;
-constexpr int kLptMaxRanksPerLane = skv_internal::kLptMaxRanks / 32;
 
 // Cost-aware LPT [Split-KV §4.2]: one thread block.  (1) bitonic sort of
 // (cost, index) in shared memory by the whole block; (2) the greedy pass by a
-// single warp: lane l keeps ranks l, l+32, ... and its own best (load, rank)
-// among ranks with fewer than J chunks; each step is one warp-wide argmin.
+// single warp: the ranks' loads and chunk counts sit in shared memory, lane l
+// keeps its best (load, rank) among ranks l, l+32, ... with fewer than J chunks,
+// and each step is one warp-wide argmin (only the receiving lane rescans).
 __global__ void __launch_bounds__(kLptThreads)
 lpt_kernel(const int64_t* __restrict__ costs, int n, int P, int J,
            int32_t* __restrict__ rank_of_chunk, int32_t* __restrict__ order,
@@ -87,25 +87,28 @@ lpt_kernel(const int64_t* __restrict__ costs, int n, int P, int J,
             __syncthreads();
         }
     }
+    // per-rank load and chunk count in shared memory, behind the sorted keys
+    int64_t* rload = reinterpret_cast<int64_t*>(smem_raw + ((size_t(n2) * 12 + 7) & ~size_t(7)));
+    int32_t* rheld = reinterpret_cast<int32_t*>(rload + P);
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        rload[p] = 0;
+        rheld[p] = 0;
+    }
+    __syncthreads();
     if (threadIdx.x >= 32) return;
     const int lane = threadIdx.x;
-    int64_t load[kLptMaxRanksPerLane];
-    int held[kLptMaxRanksPerLane];
-    const int rpl = (P + 31) / 32;
-#pragma unroll
-    for (int r = 0; r < kLptMaxRanksPerLane; ++r) { load[r] = 0; held[r] = 0; }
     constexpr int64_t kFull = 0x7fffffffffffffffLL;
-    // best (load, rank) of this lane among ranks that can still take a chunk
+    // best (load, rank) of this lane among its ranks lane, lane + 32, ... that can
+    // still take a chunk; only the lane that received a chunk rescans its ranks
     int64_t best_load = kFull;
     int best_rank = 0x7fffffff;
     auto refresh = [&]() {
         best_load = kFull;
         best_rank = 0x7fffffff;
-#pragma unroll
-        for (int r = 0; r < kLptMaxRanksPerLane; ++r) {
-            const int p = lane + 32 * r;
-            if (r < rpl && p < P && held[r] < J && load[r] < best_load) {
-                best_load = load[r];
+        for (int p = lane; p < P; p += 32) {
+            const int64_t l = rload[p];
+            if (rheld[p] < J && l < best_load) {
+                best_load = l;
                 best_rank = p;
             }
         }
@@ -124,24 +127,15 @@ lpt_kernel(const int64_t* __restrict__ costs, int n, int P, int J,
         }
         if (br == 0x7fffffff) break;   // unreachable when n == P*J
         if ((br & 31) == lane) {
-            const int r = br >> 5;
-#pragma unroll
-            for (int rr = 0; rr < kLptMaxRanksPerLane; ++rr) {
-                if (rr == r) {
-                    order[int64_t(br) * J + held[rr]] = j;
-                    load[rr] += c;
-                    held[rr] += 1;
-                }
-            }
+            order[int64_t(br) * J + rheld[br]] = j;
+            rload[br] += c;
+            rheld[br] += 1;
             rank_of_chunk[j] = br;
             refresh();
         }
     }
-#pragma unroll
-    for (int r = 0; r < kLptMaxRanksPerLane; ++r) {
-        const int p = lane + 32 * r;
-        if (r < rpl && p < P) load_out[p] = load[r];
-    }
+    __syncwarp();
+    for (int p = lane; p < P; p += 32) load_out[p] = rload[p];
 }
 
 __global__ void contiguous_kernel(const int64_t* __restrict__ costs, int n, int P, int J,
@@ -254,7 +248,9 @@ skv_status launch_lpt(const int64_t* costs, int n, int P, int J, int32_t* roc, i
                       int64_t* load, const skv_host::Ctx& c) {
     int n2 = 1;
     while (n2 < n) n2 <<= 1;
-    const size_t smem = size_t(n2) * (sizeof(int64_t) + sizeof(int32_t));
+    // sorted (cost, index) pairs, then each rank's load and chunk count
+    const size_t smem = ((size_t(n2) * (sizeof(int64_t) + sizeof(int32_t)) + 7) & ~size_t(7)) +
+                        size_t(P) * (sizeof(int64_t) + sizeof(int32_t));
     SKV_CUDA_CHECK(cudaFuncSetAttribute(lpt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     lpt_kernel<<<1, kLptThreads, smem, c.stream>>>(costs, n, P, J, roc, order, load);
     SKV_LAUNCHED();
