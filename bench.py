@@ -632,30 +632,32 @@ def run_ours(args):
         torch.cuda.synchronize()
         serial_ms = t_s.elapsed_time(t_e) / ke
 
-        # pipelined: the inputs have two device sets (the resident one and a second),
-        # the results one (the resident buffers).  Step t+1's inputs go up on one copy
-        # stream while step t computes; step t's results come down on another while
-        # step t+1 plans and runs its forward; step t+1's merge and backward wait
-        # until the results they overwrite are down.  Every step still copies all of
-        # its inputs in and all of its results out.
+        # pipelined: the inputs and the results each have two device sets (the resident
+        # one and a second).  Step t+1's inputs go up on one copy stream while step t
+        # computes; step t's results come down on another while step t+1 computes into
+        # the other result set.  A set is reused two steps later, once its inputs have
+        # been read and its results are down.  Every step still copies all of its
+        # inputs in and all of its results out.
         names_in = ("s", "a", "q", "k", "v", "dO")
         in_sets = [dict(zip(names_in, (s, a, q, k, v, dO)))]
         in_sets.append({nm: torch.empty_like(x) for nm, x in in_sets[0].items()})
         probs = [skv.Problem(st["s"], st["a"], w.B, H, d, w.S, w.m, P, tdt, n_kv_heads=w.Hkv) for st in in_sets]
         h_src = [hsrc for hsrc, _ in h_in]
-        h_small = [(o, h_o), (lse, h_lse)]
-        h_big = [(dq, h_dq), (dk, h_dk), (dv, h_dv)]
+        out_sets = [(o, lse, dq, dk, dv)]
+        out_sets.append(tuple(torch.empty_like(x) for x in out_sets[0]))
+        h_dst = (h_o, h_lse, h_dq, h_dk, h_dv)
         up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         comp = torch.cuda.current_stream(dev)
         ev_in = [torch.cuda.Event() for _ in range(2)]
         ev_used = [torch.cuda.Event() for _ in range(2)]
-        ev_done, ev_small, ev_big = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
-        started = [False]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_down = [torch.cuda.Event() for _ in range(2)]
 
         def pipelined(n_steps):
             for t in range(n_steps):
                 b = t % 2
                 st, pr = in_sets[b], probs[b]
+                o_b, lse_b, dq_b, dk_b, dv_b = out_sets[b]
                 with torch.cuda.stream(up):
                     up.wait_event(ev_used[b])            # step t-2 has finished with these inputs
                     for hs, nm in zip(h_src, names_in):
@@ -668,23 +670,16 @@ def run_ours(args):
                 else:
                     roc_s, _, _ = skv.contiguous_order(w.n_chunks, P, w.J, costs)
                 skv.attn_fwd(pr, st["q"], st["k"], st["v"], roc_s, o_part[:P], lse_part[:P], ws_f)
-                if started[0]:
-                    comp.wait_event(ev_small)            # step t-1's o and lse are down
-                skv.lse_merge(o_part[:P], lse_part[:P], o=o, lse=lse)
-                if started[0]:
-                    comp.wait_event(ev_big)              # step t-1's dq, dk and dv are down
-                skv.attn_bwd(pr, st["q"], st["k"], st["v"], o, lse, st["dO"], roc_s, dq, dk, dv, ws_b)
+                comp.wait_event(ev_down[b])              # step t-2's results are down
+                skv.lse_merge(o_part[:P], lse_part[:P], o=o_b, lse=lse_b)
+                skv.attn_bwd(pr, st["q"], st["k"], st["v"], o_b, lse_b, st["dO"], roc_s, dq_b, dk_b, dv_b, ws_b)
                 ev_used[b].record(comp)
-                ev_done.record(comp)
-                started[0] = True
+                ev_done[b].record(comp)
                 with torch.cuda.stream(down):
-                    down.wait_event(ev_done)
-                    for dsrc, hdst in h_small:
+                    down.wait_event(ev_done[b])
+                    for dsrc, hdst in zip(out_sets[b], h_dst):
                         hdst.copy_(dsrc, non_blocking=True)
-                    ev_small.record(down)
-                    for dsrc, hdst in h_big:
-                        hdst.copy_(dsrc, non_blocking=True)
-                    ev_big.record(down)
+                    ev_down[b].record(down)
             comp.wait_stream(up)
             comp.wait_stream(down)
 
@@ -698,15 +693,14 @@ def run_ours(args):
         if skv.stream_status() != 0:
             raise RuntimeError("device status set during the end-to-end pass")
         e_ms = t_s.elapsed_time(t_e) / kp
-        del in_sets, probs, h_in, h_small, h_big, h_src, h_out, h_o, h_lse, h_dq, h_dk, h_dv
+        del in_sets, probs, out_sets, h_in, h_src, h_dst, h_out, h_o, h_lse, h_dq, h_dk, h_dv
         e_ms, serial_ms = slowest([e_ms, serial_ms], world, dev)
         e2e = {"value": job_tflops(step_flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "mode": f"pipelined over {kp} steps: step t+1's inputs go up on one copy stream while "
-                       "step t computes (two device input sets), step t's results come down on another "
-                       "while step t+1 plans and runs its forward (one result set: step t+1's merge and "
-                       "backward wait for that download); the first upload and the last download are "
-                       "inside the timed region",
+                       "step t computes, step t's results come down on another while step t+1 computes "
+                       "(two device sets of inputs and of results, each reused two steps later); the "
+                       "first upload and the last download are inside the timed region",
                "serial": {"ms_per_step": serial_ms, "value": job_tflops(step_flops, world, serial_ms)}}
 
     if rank == 0:
