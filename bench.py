@@ -146,7 +146,7 @@ class ClockSampler:
             self.proc.kill()
         if self.t:
             self.t.join(timeout=2)
-        sms, mx, reasons = [], None, set()
+        sms, mx, reasons, watts = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
@@ -157,13 +157,20 @@ class ClockSampler:
                 mx = float(parts[2])
             except ValueError:
                 continue
+            try:
+                watts.append(float(parts[3]))
+            except ValueError:
+                pass
             for nm, val in zip(names, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(nm)
         if not sms:
             return None
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sms)}
+        out = {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons),
+               "samples": len(sms)}
+        if watts:
+            out["power_w"] = statistics.median(watts)
+        return out
 
 
 def useful_pairs_per_head(s, a, B):
