@@ -16,7 +16,7 @@
 // miss both tiles' windows only marks their rows empty.
 //
 // The two query tiles share every K/V tile and alternate on the tensor core,
-// so one tile's exponentials overlap the other tile's MMAs.  Roles (320 threads):
+// so one tile's exponentials overlap the other tile's MMAs.  Roles (384 threads):
 //   warps 0-3, 4-7  softmax of query tile 0, 1: thread owns one row; reads S
 //                   from TMEM, online max / exp2 / sum, bf16 P back to TMEM (over
 //                   S), rescales O when the running max grows by more than 2^8.
