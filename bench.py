@@ -700,6 +700,16 @@ def run_ours(args):
         if skv.stream_status() != 0:
             raise RuntimeError("device status set during the end-to-end pass")
         e_ms = t_s.elapsed_time(t_e) / kp
+        # Every step had the same inputs, and the kernels are deterministic: the last
+        # step's host copies equal its device set, and both device sets agree (bit for
+        # bit, on rows sampled evenly over each result).
+        b_last = (kp - 1) % 2
+        for x0, x1, hx in zip(out_sets[0], out_sets[1], h_dst):
+            idx = torch.linspace(0, x0.shape[0] - 1, steps=min(x0.shape[0], 4096)).long()
+            idx_d = idx.to(dev)
+            got = (x0, x1)[b_last][idx_d].cpu()
+            if not (torch.equal(got, hx[idx]) and torch.equal(x0[idx_d], x1[idx_d])):
+                raise RuntimeError("end-to-end results differ from the device-resident results")
         del in_sets, probs, out_sets, h_in, h_src, h_dst, h_out, h_o, h_lse, h_dq, h_dk, h_dv
         e_ms, serial_ms = slowest([e_ms, serial_ms], world, dev)
         e2e = {"value": job_tflops(step_flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
