@@ -80,6 +80,18 @@ def merge_algorithmic_bytes(lse_merged, d: int, out_b: int) -> int:
     return P * rows * 4 + finite * d * 4 + rows * (d * out_b + 4)
 
 
+def host_mem_available():
+    """MemAvailable of /proc/meminfo in bytes, or None where it cannot be read."""
+    try:
+        with open("/proc/meminfo", encoding="ascii") as fh:
+            for ln in fh:
+                if ln.startswith("MemAvailable:"):
+                    return int(ln.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    return None
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -610,7 +622,23 @@ def run_ours(args):
 
     # end to end through the public API with host buffers (pinned), copies inside
     e2e = None
+    e2e_fits = True
     if not args.no_e2e and w.backward:
+        # the pinned host buffers of every rank on this node must fit in its free memory
+        # (all ranks take the same decision)
+        need = sum(x.numel() * x.element_size() for x in (s, a, q, k, v, dO, o, lse, dq, dk, dv))
+        peak = need + max(x.numel() * x.element_size() for x in (q, k, v, dO))   # + one pageable staging copy
+        local_world = int(os.environ.get("LOCAL_WORLD_SIZE", str(world)))
+        avail = host_mem_available()
+        e2e_fits = avail is None or peak * local_world <= avail
+        if world > 1:
+            flag = torch.tensor([1 if e2e_fits else 0], device=dev)
+            dist.all_reduce(flag, op=dist.ReduceOp.MIN)
+            e2e_fits = bool(flag.item())
+        if not e2e_fits:
+            e2e = {"skipped": f"the pinned host buffers ({need / 1e9:.0f} GB a rank, {local_world} ranks on this "
+                              f"node) exceed the host memory available ({(avail or 0) / 1e9:.0f} GB)"}
+    if not args.no_e2e and w.backward and e2e_fits:
         h_o = torch.empty(Q, H, d, dtype=tdt, pin_memory=True)
         h_lse = torch.empty(Q, H, dtype=torch.float32, pin_memory=True)
         h_dq = torch.empty(Q, H, d, dtype=torch.float32, pin_memory=True)
