@@ -92,6 +92,13 @@ def host_mem_available():
     return None
 
 
+def pinned_buffers_fit(need: int, staging: int, ranks_on_node: int, avail) -> bool:
+    """Whether every rank of a node can pin its end-to-end buffers (need bytes)
+    beside one pageable staging copy, within the node's available host memory
+    (None: unknown, assumed to fit)."""
+    return avail is None or (need + staging) * ranks_on_node <= avail
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -627,10 +634,10 @@ def run_ours(args):
         # the pinned host buffers of every rank on this node must fit in its free memory
         # (all ranks take the same decision)
         need = sum(x.numel() * x.element_size() for x in (s, a, q, k, v, dO, o, lse, dq, dk, dv))
-        peak = need + max(x.numel() * x.element_size() for x in (q, k, v, dO))   # + one pageable staging copy
+        staging = max(x.numel() * x.element_size() for x in (q, k, v, dO))   # one pageable copy at a time
         local_world = int(os.environ.get("LOCAL_WORLD_SIZE", str(world)))
         avail = host_mem_available()
-        e2e_fits = avail is None or peak * local_world <= avail
+        e2e_fits = pinned_buffers_fit(need, staging, local_world, avail)
         if world > 1:
             flag = torch.tensor([1 if e2e_fits else 0], device=dev)
             dist.all_reduce(flag, op=dist.ReduceOp.MIN)

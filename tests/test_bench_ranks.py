@@ -93,3 +93,14 @@ def test_traffic_digest_follows_code_not_comments(tmp_path, monkeypatch):
     assert bench.csrc_digest() == base
     f0.write_text(text + "\nstatic const int digest_probe = 1;\n")   # one line of code more
     assert bench.csrc_digest() != base
+
+
+def test_pinned_buffer_check():
+    # the default workload's 106 GB of pinned buffers and its 17 GB staging copy fit one
+    # rank on a 199 GB box, not eight ranks; an unreadable meminfo does not block the pass
+    need, staging = 105_800_000_000, 17_200_000_000
+    assert bench.pinned_buffers_fit(need, staging, 1, 190_000_000_000)
+    assert not bench.pinned_buffers_fit(need, staging, 8, 900_000_000_000)
+    assert bench.pinned_buffers_fit(need, staging, 8, None)
+    avail = bench.host_mem_available()
+    assert avail is None or avail > 0
