@@ -66,7 +66,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
     }
 }
 
-// The same wait made by every lane of a converged warp, with one verdict for
+// The same wait made by every lane of a converged warp, with one outcome for
 // all lanes (all lanes polling measured faster than one lane plus a shuffle).
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, long long limit_ns,
                                                const int* abort_flag = nullptr) {
